@@ -1,0 +1,180 @@
+/*
+ * lowm_gemm.h -- C ABI of the GB300 (sm_103a) low-M split-K bf16 GEMM.
+ *
+ * The library computes
+ *
+ *     C[M,N] = A[M,K] . W[N,K]^T        bf16 inputs, fp32 accumulation, bf16 output
+ *
+ * for small M (1..64): a weight matrix W is streamed once from HBM while the
+ * few activation rows A are reused by every CTA.  This is the operation of the
+ * low-M split-K GEMM described in the TensorRT-LLM PR "Fix two synchronization
+ * gaps in the MiniMax M3 low-M split-K GEMM" (Description; Hardware
+ * verification): K is split across the CTAs of one thread-block cluster, the
+ * non-owner ranks push their fp32 partial tiles into the owner's (rank 0's)
+ * shared-memory mailbox with st.async + complete_tx, and rank 0 sums them in
+ * rank order, converts to bf16 and stores.
+ *
+ * Conventions shared by every entry point:
+ *   - Layouts: A row-major [M,K] (K contiguous), W row-major [N,K] (K
+ *     contiguous, i.e. the K-major weight), C row-major [M,N].  All three are
+ *     bf16 (IEEE binary32 upper halves), passed as plain device pointers unless
+ *     the name says "host".
+ *   - Ownership: the caller owns every buffer.  No entry point allocates or
+ *     frees device memory.  The library keeps only process-wide state: a small
+ *     cache of TMA descriptors, per-kernel attribute flags, and one device
+ *     status word (a module global).
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Calls enqueue work and return; they do not synchronize
+ *     (except lowm_gemm_sync_status and lowm_gemm_bf16_host, as documented).
+ *   - Errors: argument checks run before anything is enqueued; a rejected call
+ *     writes nothing and launches nothing.  A CUDA runtime failure maps to
+ *     LOWM_ERR_CUDA.  Kernel-side timeouts (a bounded wait that gave up) are
+ *     recorded in the device status word and reported by
+ *     lowm_gemm_sync_status.  No C++ exception crosses this boundary.
+ *   - Threads: entry points may be called from several host threads; the
+ *     descriptor cache is locked internally.
+ *   - Device: the current CUDA device must be compute capability 10.3
+ *     (GB300); otherwise LOWM_ERR_UNSUPPORTED_ARCH.
+ */
+#ifndef LOWM_GEMM_H
+#define LOWM_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LOWM_OK = 0,
+    LOWM_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative or zero size, bad option */
+    LOWM_ERR_UNSUPPORTED_SHAPE = 2,  /* a shape rule below is broken */
+    LOWM_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+    LOWM_ERR_UNSUPPORTED_ARCH = 4,   /* the current device is not sm_103 */
+    LOWM_ERR_CUDA = 5,               /* a CUDA runtime call failed */
+    LOWM_ERR_TIMEOUT = 6             /* a kernel's bounded wait gave up (see lowm_gemm_sync_status) */
+} lowm_status_t;
+
+/*
+ * A tactic: how one GEMM is tiled and launched.
+ *   tile_n       output columns per CTA; the MMA's M dimension (swap-AB: N is
+ *                mapped onto the tensor core's M, the tiny M onto its N)
+ *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32 or 64);
+ *                rows M..m_pad-1 are zero-filled by the TMA unit and never stored
+ *   split_k      CTAs per cluster along K (1, 2, 4 or 8)
+ *   stages       depth of the shared-memory ring between the TMA producer and the MMA warp
+ *   block_k      K elements per ring stage (64: one 128-byte swizzle row of bf16)
+ *   num_clusters N / tile_n
+ *   ctas         num_clusters * split_k
+ *   smem_bytes   dynamic shared memory requested per CTA
+ *   pdl          1 when launched with programmatic dependent launch
+ * The pages' shipped tactic reads as (tile_n 64, m_pad 8, split_k 2, stages 10)
+ * ("Fix two synchronization gaps ...", Hardware verification).
+ */
+typedef struct {
+    int tile_n, m_pad, split_k, stages, block_k;
+    int num_clusters, ctas, smem_bytes, pdl;
+} lowm_tactic_t;
+
+/*
+ * C = A . W^T on `stream`.
+ *   M        1..64
+ *   N        a positive multiple of 64
+ *   K        a positive multiple of split_k * 64
+ *   split_k  0 (let the tactic table choose), 1, 2, 4 or 8
+ *   A, W, C  device pointers, 16-byte aligned; C must not overlap A or W
+ * Returns LOWM_OK once the kernel is enqueued.
+ */
+lowm_status_t lowm_gemm_bf16(const void *A, const void *W, void *C,
+                             int M, int N, int K, int split_k, void *stream);
+
+/*
+ * Fill *out with the tactic lowm_gemm_bf16 would launch for these arguments
+ * (host only; no device work).  Same argument rules and status codes as
+ * lowm_gemm_bf16, minus the pointer checks.
+ */
+lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tactic_t *out);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char *lowm_status_string(lowm_status_t status);
+
+/*
+ * Synchronize `stream`, then read and clear the device status word that the
+ * kernels set when a bounded wait gives up.  Returns LOWM_ERR_TIMEOUT if any
+ * kernel since the last call recorded one (the word's bits are written to
+ * *detail when detail is non-NULL), LOWM_ERR_CUDA if synchronization failed,
+ * else LOWM_OK.
+ */
+lowm_status_t lowm_gemm_sync_status(void *stream, unsigned int *detail);
+
+/*
+ * End-to-end form for callers whose operands live in host memory: copies
+ * A_host and W_host into the caller-provided device buffers A_dev and W_dev,
+ * runs lowm_gemm_bf16 into C_dev, copies C_dev back into C_host, all on
+ * `stream`, then synchronizes `stream`.  Host buffers should be pinned for
+ * asynchronous copies; pageable memory works but serializes.  Sizes follow
+ * from M, N, K (A: M*K*2 bytes, W: N*K*2, C: M*N*2).
+ */
+lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *C_host,
+                                  void *A_dev, void *W_dev, void *C_dev,
+                                  int M, int N, int K, int split_k, void *stream);
+
+/*
+ * Test and tuning hooks.  The race-stress method of the pages ("Fix two
+ * synchronization gaps ...", Hardware verification): stall some epilogue
+ * warps before their first arrival on the TMEM barrier, keep the shared
+ * memory request at the kernel's footprint so another kernel can co-reside
+ * on the SM, run a TMEM-allocating kernel on a second stream, and probe
+ * %globaltimer at the epilogue's tcgen05.ld and the MMA warp's tcgen05.dealloc.
+ *
+ *   stall_warp_mask  bit w set: warp w of the CTA (epilogue warps are 2..5)
+ *                    sleeps stall_ns before its first TMEM-barrier arrival
+ *   stall_rank_mask  bit r set: only cluster ranks r stall (0 = every rank)
+ *   stall_ns         stall length in nanoseconds (bounded busy sleep)
+ *   full_smem        0: request the kernel's footprint (the default, which
+ *                    lets another kernel co-reside on the SM); 1: request the
+ *                    full 227 KiB per CTA as the pages' shipped launch does,
+ *                    so nothing else can co-reside
+ *   stages           0: tactic default; else the ring depth to use (>= 2)
+ *   drop_mailbox     1: the non-owner ranks skip their mailbox publication, so
+ *                    the owner's mailbox wait runs out (a dropped message, to
+ *                    test the timeout path); the output is then undefined
+ *   reduce_timeout_ns 0: default (2 s); else the bound on the owner's
+ *                    mailbox wait.  Every other wait keeps its 2 s bound.
+ *   probes           NULL, or device u64[2 * ctas]: per CTA (by linear CTA
+ *                    index) [0] = latest %globaltimer after any epilogue
+ *                    thread's tcgen05.wait::ld, [1] = %globaltimer just before
+ *                    tcgen05.dealloc.  Zero-initialise before the launch.
+ *   c_f32            NULL, or device float[M*N]: the fp32 sums before the bf16
+ *                    rounding (written by the owner rank)
+ */
+typedef struct {
+    unsigned int stall_warp_mask;
+    unsigned int stall_rank_mask;
+    unsigned int stall_ns;
+    int full_smem;
+    int stages;
+    int drop_mailbox;
+    unsigned long long reduce_timeout_ns;
+    unsigned long long *probes;
+    float *c_f32;
+} lowm_debug_opts_t;
+
+/* lowm_gemm_bf16 with the hooks above (opts may be NULL: same as lowm_gemm_bf16). */
+lowm_status_t lowm_gemm_bf16_debug(const void *A, const void *W, void *C,
+                                   int M, int N, int K, int split_k, void *stream,
+                                   const lowm_debug_opts_t *opts);
+
+/*
+ * The concurrent TMEM allocator of the stress method: `ctas` CTAs, each
+ * allocates `ncols` TMEM columns (32..256, a power of two), writes NaN into
+ * every lane of them `iters` times, frees them and exits.  It never waits on
+ * another kernel.  Enqueued on `stream`.
+ */
+lowm_status_t lowm_tmem_hog_launch(void *stream, int ctas, int ncols, int iters);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOWM_GEMM_H */

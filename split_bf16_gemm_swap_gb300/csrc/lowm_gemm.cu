@@ -1,0 +1,454 @@
+// Host side of the C ABI in include/lowm_gemm.h: argument checks, the tactic
+// table, TMA descriptor encoding (cached), and the cluster + PDL launch.
+//
+// Launch shape ("Fix two synchronization gaps in the MiniMax M3 low-M split-K
+// GEMM", TensorRT-LLM PR, Hardware verification): N / 64 clusters of split_k
+// CTAs, programmatic dependent launch on, cluster dimension split_k along grid
+// x.  The host also guarantees the non-empty K loop that the PR's analysis of
+// the TMEM race relies on (Description, item 1): K must be a positive
+// multiple of split_k * 64.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/lowm_gemm.h"
+#include "lowm_kernel.cuh"
+
+namespace {
+
+using lowm::KernelParams;
+using lowm::SmemLayout;
+
+constexpr int kMaxSmemPerCta = 232448;     // 227 KiB opt-in dynamic shared memory per CTA
+constexpr int kSmemPerSm = 233472;         // 228 KiB per SM
+constexpr int kSmemReservedPerCta = 1024;  // the runtime keeps 1 KiB per resident CTA
+
+// ------------------------------------------------------------------ driver entry point
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// ------------------------------------------------------------------ device checks
+struct DeviceInfo {
+    bool checked = false;
+    bool ok = false;
+    int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+lowm_status_t check_device(int *sms_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return LOWM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return LOWM_ERR_CUDA;
+        d.ok = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.checked = true;
+    }
+    if (sms_out)
+        *sms_out = d.sms;
+    return d.ok ? LOWM_OK : LOWM_ERR_UNSUPPORTED_ARCH;
+}
+
+// ------------------------------------------------------------------ tactics
+int m_pad_of(int M)
+{
+    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
+}
+
+int footprint(int m_pad, int split_k, int stages)
+{
+    return (int)lowm::make_smem_layout(m_pad, split_k, stages).bytes;
+}
+
+// Deepest ring that lets `ctas_per_sm` CTAs share one SM.
+int stages_for(int m_pad, int split_k, int ctas_per_sm)
+{
+    const int budget = kSmemPerSm / ctas_per_sm - kSmemReservedPerCta;
+    int s = 2;
+    while (s < 32 && footprint(m_pad, split_k, s + 1) <= budget && footprint(m_pad, split_k, s + 1) <= kMaxSmemPerCta)
+        ++s;
+    return s;
+}
+
+bool shape_ok(int M, int N, int K, int split_k)
+{
+    return M >= 1 && M <= 64 && N > 0 && N % lowm::kTileN == 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
+}
+
+// split_k = 0: the smallest split (1, 2, 4, 8) that keeps the K loop non-empty
+// and gives at least one CTA per SM, preferring fewer cluster reductions.
+int choose_split_k(int M, int N, int K, int sms)
+{
+    (void)M;
+    const int tiles = N / lowm::kTileN;
+    int best = 0;
+    for (int sk = 1; sk <= 8; sk *= 2) {
+        if (K % (sk * lowm::kBlockK) != 0)
+            break;
+        best = sk;
+        if (tiles * sk >= sms)
+            break;
+    }
+    return best;
+}
+
+lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, int stages_override, int full_smem,
+                          lowm_tactic_t *t)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || split_k < 0)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (split_k == 0)
+        split_k = choose_split_k(M, N, K, sms > 0 ? sms : 152);
+    if (split_k == 0 || !shape_ok(M, N, K, split_k))
+        return LOWM_ERR_UNSUPPORTED_SHAPE;
+    const int m_pad = m_pad_of(M);
+    // Two CTAs per SM by default: one CTA's prologue and epilogue overlap the
+    // other's stream, and the next kernel's CTAs (PDL) can start early.
+    int stages = stages_override > 0 ? stages_override : stages_for(m_pad, split_k, 2);
+    if (stages < 2)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    const int fp = footprint(m_pad, split_k, stages);
+    if (fp > kMaxSmemPerCta)
+        return LOWM_ERR_UNSUPPORTED_SHAPE;
+    t->tile_n = lowm::kTileN;
+    t->m_pad = m_pad;
+    t->split_k = split_k;
+    t->stages = stages;
+    t->block_k = lowm::kBlockK;
+    t->num_clusters = N / lowm::kTileN;
+    t->ctas = t->num_clusters * split_k;
+    t->smem_bytes = full_smem ? kMaxSmemPerCta : fp;
+    t->pdl = 1;
+    return LOWM_OK;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+struct MapKey {
+    uintptr_t ptr;
+    int rows, K, box_rows;
+    bool operator==(const MapKey &o) const
+    {
+        return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        size_t h = std::hash<uintptr_t>()(k.ptr);
+        h ^= std::hash<long long>()(((long long)k.rows << 32) ^ ((long long)k.K << 8) ^ k.box_rows) + 0x9e3779b9 +
+             (h << 6) + (h >> 2);
+        return h;
+    }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;   // guarded by g_mu
+
+// 2-D map over a row-major [rows, K] bf16 matrix, box [box_rows, 64], 128-byte swizzle.
+lowm_status_t get_map(const void *ptr, int rows, int K, int box_rows, CUtensorMap *out)
+{
+    const MapKey key{reinterpret_cast<uintptr_t>(ptr), rows, K, box_rows};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return LOWM_OK;
+        }
+    }
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc)
+        return LOWM_ERR_CUDA;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)lowm::kBlockK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return LOWM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_maps.size() > 4096)
+        g_maps.clear();
+    g_maps.emplace(key, m);
+    *out = m;
+    return LOWM_OK;
+}
+
+// ------------------------------------------------------------------ launch
+typedef void (*KernelFn)(CUtensorMap, CUtensorMap, KernelParams);
+
+template <int MP, int SK>
+KernelFn kernel_ptr()
+{
+    return reinterpret_cast<KernelFn>(&lowm::lowm_splitk_kernel<MP, SK>);
+}
+
+template <int MP>
+KernelFn kernel_for_split(int sk)
+{
+    switch (sk) {
+    case 1: return kernel_ptr<MP, 1>();
+    case 2: return kernel_ptr<MP, 2>();
+    case 4: return kernel_ptr<MP, 4>();
+    case 8: return kernel_ptr<MP, 8>();
+    default: return nullptr;
+    }
+}
+
+KernelFn kernel_for(int m_pad, int sk)
+{
+    switch (m_pad) {
+    case 8: return kernel_for_split<8>(sk);
+    case 16: return kernel_for_split<16>(sk);
+    case 32: return kernel_for_split<32>(sk);
+    case 64: return kernel_for_split<64>(sk);
+    default: return nullptr;
+    }
+}
+
+lowm_status_t prepare_kernel(KernelFn fn)
+{
+    // Opt every instance into the largest request once per device.
+    static std::mutex mu;
+    static std::unordered_map<long long, bool> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    const long long key = (long long)reinterpret_cast<uintptr_t>(fn) * 64 + dev;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(key))
+        return LOWM_OK;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxSmemPerCta) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    done[key] = true;
+    return LOWM_OK;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K, int split_k, void *stream,
+                     const lowm_debug_opts_t *dbg)
+{
+    if (!A || !W || !C)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (M <= 0 || N <= 0 || K <= 0)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (!aligned16(A) || !aligned16(W) || !aligned16(C))
+        return LOWM_ERR_MISALIGNED;
+    const size_t a_bytes = (size_t)M * K * 2, w_bytes = (size_t)N * K * 2, c_bytes = (size_t)M * N * 2;
+    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, W, w_bytes))
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (dbg && (dbg->stages == 1 || dbg->stages < 0))
+        return LOWM_ERR_INVALID_ARGUMENT;
+    int sms = 0;
+    lowm_status_t st = check_device(&sms);
+    if (st != LOWM_OK)
+        return st;
+    lowm_tactic_t t;
+    st = make_tactic(M, N, K, split_k, sms, dbg ? dbg->stages : 0, (dbg && dbg->full_smem) ? 1 : 0, &t);
+    if (st != LOWM_OK)
+        return st;
+    KernelFn fn = kernel_for(t.m_pad, t.split_k);
+    if (!fn)
+        return LOWM_ERR_UNSUPPORTED_SHAPE;
+    if ((st = prepare_kernel(fn)) != LOWM_OK)
+        return st;
+    CUtensorMap map_a, map_w;
+    if ((st = get_map(A, M, K, t.m_pad, &map_a)) != LOWM_OK)
+        return st;
+    if ((st = get_map(W, N, K, lowm::kTileN, &map_w)) != LOWM_OK)
+        return st;
+
+    KernelParams p;
+    std::memset(&p, 0, sizeof p);
+    p.C = reinterpret_cast<__nv_bfloat16 *>(C);
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.stages = t.stages;
+    p.kb_per_rank = K / (t.split_k * lowm::kBlockK);
+    p.timeout_ns = lowm::kDefaultTimeoutNs;
+    p.reduce_timeout_ns = lowm::kDefaultTimeoutNs;
+    if (dbg) {
+        p.stall_warp_mask = dbg->stall_warp_mask;
+        p.stall_rank_mask = dbg->stall_rank_mask;
+        p.stall_ns = dbg->stall_ns;
+        p.drop_mailbox = dbg->drop_mailbox ? 1u : 0u;
+        p.probes = dbg->probes;
+        p.c_f32 = dbg->c_f32;
+        if (dbg->reduce_timeout_ns)
+            p.reduce_timeout_ns = dbg->reduce_timeout_ns;
+    }
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)t.ctas, 1, 1);
+    cfg.blockDim = dim3(lowm::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)t.smem_bytes;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (t.split_k > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)t.split_k;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    if (std::getenv("LOWM_LOG"))
+        std::fprintf(stderr, "lowm: M%d N%d K%d -> tile_n %d m_pad %d split_k %d stages %d ctas %d smem %d\n", M, N,
+                     K, t.tile_n, t.m_pad, t.split_k, t.stages, t.ctas, t.smem_bytes);
+    if (cudaLaunchKernelEx(&cfg, fn, map_a, map_w, p) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    return LOWM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lowm_status_t lowm_gemm_bf16(const void *A, const void *W, void *C, int M, int N, int K, int split_k, void *stream)
+{
+    return launch(A, W, C, M, N, K, split_k, stream, nullptr);
+}
+
+lowm_status_t lowm_gemm_bf16_debug(const void *A, const void *W, void *C, int M, int N, int K, int split_k,
+                                   void *stream, const lowm_debug_opts_t *opts)
+{
+    return launch(A, W, C, M, N, K, split_k, stream, opts);
+}
+
+lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tactic_t *out)
+{
+    if (!out)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    int sms = 152;   // host-only query: use the device's count when one is current and usable
+    int dev = 0, n = 0;
+    if (cudaGetDeviceCount(&n) == cudaSuccess && n > 0 && cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    else
+        cudaGetLastError();
+    lowm_tactic_t t;
+    const lowm_status_t st = make_tactic(M, N, K, split_k, sms, 0, 0, &t);
+    if (st == LOWM_OK)
+        *out = t;
+    return st;
+}
+
+const char *lowm_status_string(lowm_status_t s)
+{
+    switch (s) {
+    case LOWM_OK: return "ok";
+    case LOWM_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=64, N%64==0, K%(split_k*64)==0)";
+    case LOWM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case LOWM_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103 (GB300)";
+    case LOWM_ERR_CUDA: return "CUDA runtime error";
+    case LOWM_ERR_TIMEOUT: return "a kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+lowm_status_t lowm_gemm_sync_status(void *stream, unsigned int *detail)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(&v, lowm::g_lowm_status, sizeof v) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(lowm::g_lowm_status, &zero, sizeof zero) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    if (detail)
+        *detail = v;
+    return v ? LOWM_ERR_TIMEOUT : LOWM_OK;
+}
+
+lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *C_host, void *A_dev, void *W_dev,
+                                  void *C_dev, int M, int N, int K, int split_k, void *stream)
+{
+    if (!A_host || !W_host || !C_host || !A_dev || !W_dev || !C_dev)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (M <= 0 || N <= 0 || K <= 0)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    lowm_tactic_t t;
+    int sms = 0;
+    lowm_status_t st = check_device(&sms);
+    if (st != LOWM_OK)
+        return st;
+    if ((st = make_tactic(M, N, K, split_k, sms, 0, 0, &t)) != LOWM_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(A_dev, A_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(W_dev, W_host, (size_t)N * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    if ((st = launch(A_dev, W_dev, C_dev, M, N, K, split_k, stream, nullptr)) != LOWM_OK)
+        return st;
+    if (cudaMemcpyAsync(C_host, C_dev, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return LOWM_ERR_CUDA;
+    return LOWM_OK;
+}
+
+lowm_status_t lowm_tmem_hog_launch(void *stream, int ctas, int ncols, int iters)
+{
+    if (ctas <= 0 || iters < 0 || ncols < 32 || ncols > 256 || (ncols & (ncols - 1)) != 0)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    lowm_status_t st = check_device(nullptr);
+    if (st != LOWM_OK)
+        return st;
+    lowm::tmem_hog_kernel<<<ctas, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ncols, iters);
+    return cudaGetLastError() == cudaSuccess ? LOWM_OK : LOWM_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,450 @@
+// The low-M split-K bf16 GEMM kernel for sm_103a:  C[M,N] = A[M,K] . W[N,K]^T.
+//
+// One CTA owns a 64-column slice of C (tile_n = 64) and 1/split_k of K.  The
+// split_k CTAs of a slice form one thread-block cluster along grid x; rank 0
+// of the cluster is the owner that reduces and stores.  Warp roles:
+//   warp 0      TMA producer: streams W tiles [64 n x 64 k] and A tiles
+//               [m_pad x 64 k] into a ring of `stages` shared-memory stages
+//               (full/empty mbarrier pair per stage).
+//   warp 1      MMA warp: allocates TMEM, issues tcgen05.mma (swap-AB: the W
+//               tile is the MMA's A operand with M = 64, the activation tile
+//               is its B operand with N = m_pad), releases each stage with
+//               tcgen05.commit, and frees TMEM after the epilogue's loads.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, split-K
+//               exchange through the owner's shared-memory mailbox, fp32 ->
+//               bf16 and 16-byte stores of C.
+//
+// Sources for the method ("Fix two synchronization gaps in the MiniMax M3
+// low-M split-K GEMM", TensorRT-LLM PR):
+//   - Description, item 1: the TMEM barrier bar_tmem_alloc with 160 arrivals
+//     (32 MMA-warp lanes + 128 epilogue threads) and two phases; the fix makes
+//     the MMA warp observe phase 0 before its release arrival.
+//   - Description, item 2: peers publish fp32 partials with
+//     st.async ... complete_tx into rank 0's shared memory, crediting
+//     bar_reduce; rank 0 waits with a relaxed cluster-scope parity wait and
+//     then one fence.acquire.sync_restrict::shared::cluster.cluster.
+//   - Hardware verification: the shipped tactic (64, 8, 2, 10), PDL on, the
+//     stall / trimmed-request / TMEM-hog stress method and globaltimer probes.
+// The cuLA PR "Fix SM90 WY input buffer reuse before WGMMA completion" gives
+// the stage-release rule kept here: a stage is handed back to the producer
+// only by tcgen05.commit, i.e. after the MMAs that read it have completed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace lowm {
+
+constexpr int kTileN = 64;          // output columns per CTA = MMA M
+constexpr int kBlockK = 64;         // K elements per ring stage (one 128-byte swizzle row)
+constexpr int kMmaK = 16;           // K per tcgen05.mma of kind::f16
+constexpr int kThreads = 192;       // 6 warps
+constexpr int kEpilogueWarp0 = 2;   // warps 2..5; warp % 4 covers every TMEM lane quarter once
+constexpr int kEpilogueThreads = 128;
+constexpr uint32_t kWStageBytes = kTileN * kBlockK * 2;   // 8 KiB
+constexpr uint32_t kTmemBarArrivals = 32 + kEpilogueThreads;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;     // 2 s per wait on another party
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;       // 2 s for this CTA's own copies / MMAs in flight
+
+// Bits of the device status word (which wait gave up).
+enum : uint32_t {
+    kErrProducerEmpty = 1u << 0,
+    kErrProducerDrain = 1u << 1,
+    kErrMmaFull = 1u << 2,
+    kErrMmaTmemPhase0 = 1u << 3,
+    kErrMmaTmemPhase1 = 1u << 4,
+    kErrMmaAccDrain = 1u << 5,
+    kErrEpiTmemPhase0 = 1u << 6,
+    kErrEpiAccFull = 1u << 7,
+    kErrReduce = 1u << 8,
+};
+
+__device__ unsigned int g_lowm_status;   // read and cleared by lowm_gemm_sync_status
+
+struct KernelParams {
+    __nv_bfloat16 *C;
+    int M, N, K;
+    int stages;
+    int kb_per_rank;        // 64-wide K blocks per cluster rank
+    uint64_t timeout_ns;    // bound on every wait for another party
+    uint64_t reduce_timeout_ns;   // bound on the owner's mailbox wait
+    // test hooks
+    uint32_t stall_warp_mask, stall_rank_mask, stall_ns;
+    uint32_t drop_mailbox;  // non-owner ranks skip their publication (the owner's wait runs out)
+    unsigned long long *probes;
+    float *c_f32;
+};
+
+// Shared-memory carve-up (byte offsets from a 1024-aligned base).  The same
+// function sizes the launch on the host.
+struct SmemLayout {
+    uint32_t w, a, mailbox, out, bars, tmem_slot, bytes;
+};
+
+__host__ __device__ inline SmemLayout make_smem_layout(int m_pad, int split_k, int stages)
+{
+    SmemLayout L;
+    uint32_t off = 0;
+    L.w = off;
+    off += (uint32_t)stages * kWStageBytes;
+    L.a = off;                                            // m_pad * 128 is a multiple of 1024
+    off += (uint32_t)stages * (uint32_t)m_pad * 128u;
+    L.mailbox = off;                                      // [(split_k-1)][64 n][m_pad] fp32
+    off += (uint32_t)(split_k - 1) * kTileN * (uint32_t)m_pad * 4u;
+    L.out = off;                                          // [m_pad][64 n] bf16 staging for C
+    off += (uint32_t)m_pad * kTileN * 2u;
+    L.bars = off;                                         // full[stages], empty[stages], acc, tmem, reduce
+    off += (uint32_t)(2 * stages + 3) * 8u;
+    L.tmem_slot = off;
+    off += 16;
+    L.bytes = off + 1024;                                 // slack to align the dynamic base
+    return L;
+}
+
+// Shared-memory matrix descriptor for a K-major bf16 tile whose rows are 128
+// bytes, written by TMA with 128-byte swizzling: 8-row swizzle atoms of 1024
+// bytes (stride byte offset), leading byte offset unused for this layout,
+// descriptor version 1, layout type 2 = SWIZZLE_128B.  Advancing the start
+// address by 32 bytes selects the next 16-element K slice of the atom.
+__device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);            // start address        bits  0-13
+    d |= (uint64_t)(16u >> 4) << 16;                      // leading byte offset  bits 16-29
+    d |= (uint64_t)(1024u >> 4) << 32;                    // stride byte offset   bits 32-45
+    d |= (uint64_t)1 << 46;                               // version              bits 46-47
+    d |= (uint64_t)2 << 61;                               // SWIZZLE_128B         bits 61-63
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, shape M x N (M = 64 here, N = m_pad).
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int mma_m, int mma_n)
+{
+    return (1u << 4)                                      // D format: f32
+           | (1u << 7)                                    // A format: bf16
+           | (1u << 10)                                   // B format: bf16
+           | ((uint32_t)(mma_n >> 3) << 17)               // N >> 3
+           | ((uint32_t)(mma_m >> 4) << 24);              // M >> 4
+}
+
+// TMEM placement of the M = 64 (cta_group::1) accumulator: row i of D lives
+// in lane 32 * (i / 16) + i % 16, i.e. the first 16 lanes of each 32-lane
+// quarter.  An epilogue warp with quarter q therefore holds rows 16q..16q+15
+// in its threads 0..15.
+__device__ __forceinline__ bool tmem_row_of_thread(int quarter, int lane, int &row)
+{
+    row = 16 * quarter + lane;
+    return lane < 16;
+}
+
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    auto poll = [&]() {
+        return kClusterScope ? ptx::mbar_try_wait_relaxed_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (poll())
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (poll())
+                return true;
+        if (ptx::globaltimer() - t0 > timeout_ns)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void record_error(uint32_t bits)
+{
+    atomicOr(&g_lowm_status, bits);
+}
+
+template <int M_PAD, int SPLIT_K>
+__global__ void __launch_bounds__(kThreads, 1)
+    lowm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
+                       const KernelParams p)
+{
+    static_assert(M_PAD % 8 == 0 && M_PAD >= 8 && M_PAD <= 64, "m_pad is the MMA N: 8..64 in steps of 8");
+    static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
+    constexpr uint32_t kAStageBytes = M_PAD * 128u;
+    constexpr uint32_t kStageTx = kWStageBytes + kAStageBytes;
+    constexpr uint32_t kTmemCols = M_PAD <= 32 ? 32u : 64u;
+    constexpr uint32_t kSlotBytes = kTileN * M_PAD * 4u;          // one rank's fp32 partial tile
+    constexpr uint32_t kIdesc = make_idesc_bf16(kTileN, M_PAD);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemLayout L = make_smem_layout(M_PAD, SPLIT_K, p.stages);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int stages = p.stages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = SPLIT_K > 1 ? ptx::cluster_ctarank() : 0u;
+    const int n0 = (int)(blockIdx.x / SPLIT_K) * kTileN;
+    const int kb0 = (int)rank * p.kb_per_rank;
+
+    const uint32_t bar_full = sbase + L.bars;                      // + 8 * stage
+    const uint32_t bar_empty = bar_full + 8u * stages;             // + 8 * stage
+    const uint32_t bar_acc = bar_full + 16u * stages;              // accumulator complete (tcgen05.commit)
+    const uint32_t bar_tmem_alloc = bar_acc + 8u;                  // two phases, 160 arrivals each
+    const uint32_t bar_reduce = bar_acc + 16u;                     // owner's mailbox barrier
+    const uint32_t tmem_slot = sbase + L.tmem_slot;
+
+    // ---------------------------------------------------------------- prologue
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            ptx::mbar_init(bar_full + 8u * s, 1);
+            ptx::mbar_init(bar_empty + 8u * s, 1);
+        }
+        ptx::mbar_init(bar_acc, 1);
+        ptx::mbar_init(bar_tmem_alloc, kTmemBarArrivals);
+        ptx::mbar_init(bar_reduce, 1);
+        if (SPLIT_K > 1 && rank == 0)     // arm the mailbox: every peer sends one full partial tile
+            ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes);
+        ptx::fence_mbarrier_init_cluster();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmap_w);
+        ptx::prefetch_tensormap(&tmap_a);
+    }
+    if (SPLIT_K > 1) {
+        // Peers may st.async into rank 0 only after its barriers exist.
+        ptx::cluster_arrive_release();
+        ptx::cluster_wait_acquire();
+    } else {
+        __syncthreads();
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::griddep_wait();          // A (and C) may belong to the previous kernel in the stream
+            const uint64_t pol_w = ptx::policy_evict_first();   // W is streamed once
+            const uint64_t pol_a = ptx::policy_evict_last();    // A is re-read by every CTA
+            int issued = 0;
+            for (int kb = 0; kb < p.kb_per_rank; ++kb) {
+                const int s = kb % stages;
+                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+                if (!wait_bounded<false>(bar_empty + 8u * s, ph ^ 1u, p.timeout_ns)) {
+                    record_error(kErrProducerEmpty);
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(bar_full + 8u * s, kStageTx);
+                const int kx = (kb0 + kb) * kBlockK;
+                ptx::tma_load_2d(sbase + L.w + (uint32_t)s * kWStageBytes, &tmap_w, kx, n0, bar_full + 8u * s, pol_w);
+                ptx::tma_load_2d(sbase + L.a + (uint32_t)s * kAStageBytes, &tmap_a, kx, 0, bar_full + 8u * s, pol_a);
+                ++issued;
+            }
+            ptx::griddep_launch_dependents();
+            // No copy may still be landing in this CTA's shared memory when it exits:
+            // the last load on each stage must have completed.
+            for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+                if (!wait_bounded<false>(bar_full + 8u * (j % stages), (uint32_t)(j / stages) & 1u, kDrainTimeoutNs)) {
+                    record_error(kErrProducerDrain);
+                    break;
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA warp
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish_alloc_permit();       // let other CTAs on this SM allocate early
+        ptx::tcgen05_fence_before_thread_sync();
+        __syncwarp();
+        ptx::tcgen05_fence_after_thread_sync();
+        const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot);
+        ptx::mbar_arrive(bar_tmem_alloc);          // phase 0: "TMEM allocated" (32 lanes)
+
+        if (lane == 0) {
+            for (int kb = 0; kb < p.kb_per_rank; ++kb) {
+                const int s = kb % stages;
+                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+                if (!wait_bounded<false>(bar_full + 8u * s, ph, p.timeout_ns)) {
+                    record_error(kErrMmaFull);
+                    break;
+                }
+                ptx::tcgen05_fence_after_thread_sync();
+                const uint64_t adesc = make_sw128_kmajor_desc(sbase + L.w + (uint32_t)s * kWStageBytes);
+                const uint64_t bdesc = make_sw128_kmajor_desc(sbase + L.a + (uint32_t)s * kAStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / kMmaK; ++kk)      // +32 bytes of K per step: +2 in the encoded address
+                    ptx::mma_bf16_ss(tmem_d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kb | kk) != 0);
+                ptx::tcgen05_commit(bar_empty + 8u * s);           // stage free once these MMAs have read it
+            }
+            ptx::tcgen05_commit(bar_acc);                          // accumulator complete
+        }
+        __syncwarp();
+
+        // TMEM release, ordered after every epilogue tcgen05.ld + wait::ld.
+        // Phase 0 of bar_tmem_alloc is completed by exactly the 32 arrivals above
+        // and the 128 epilogue threads' first arrivals: an epilogue thread makes
+        // its second arrival only after observing phase 0, and this warp makes
+        // its second arrival only after observing phase 0 too (the wait below;
+        // without it, the arrival could still count toward phase 0, and the
+        // parity-1 wait would then test the phase before phase 0 and return at
+        // once).  Phase 1 therefore consists of these 32 second arrivals and the
+        // 128 arrivals the epilogue makes after tcgen05.wait::ld, and the
+        // parity-1 wait returns only when all of those have happened.
+        if (!wait_bounded<false>(bar_tmem_alloc, 0, p.timeout_ns))
+            record_error(kErrMmaTmemPhase0);
+        ptx::mbar_arrive(bar_tmem_alloc);          // phase 1 (32 lanes)
+        if (!wait_bounded<false>(bar_tmem_alloc, 1, p.timeout_ns))
+            record_error(kErrMmaTmemPhase1);
+        // Every MMA this CTA issued has completed before its columns are freed
+        // (already implied on the normal path, where the epilogue waited for it).
+        if (!wait_bounded<false>(bar_acc, 0, kDrainTimeoutNs))
+            record_error(kErrMmaAccDrain);
+        ptx::tcgen05_fence_after_thread_sync();
+        if (p.probes != nullptr && lane == 0) {
+            const uint64_t t = ptx::globaltimer();
+            ptx::griddep_wait();                   // the probe buffer may be written by the previous kernel
+            p.probes[2 * blockIdx.x + 1] = t;
+        }
+        __syncwarp();
+        ptx::tmem_dealloc(tmem_d, kTmemCols);
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int quarter = warp & 3;             // the TMEM lane quarter this warp may access
+        const int etid = threadIdx.x - kEpilogueWarp0 * 32;
+        if (((p.stall_warp_mask >> warp) & 1u) && (p.stall_rank_mask == 0 || ((p.stall_rank_mask >> rank) & 1u))) {
+            const uint64_t t0 = ptx::globaltimer();     // bounded stall (test hook)
+            while (ptx::globaltimer() - t0 < p.stall_ns)
+                ptx::nanosleep(256);
+        }
+        ptx::mbar_arrive(bar_tmem_alloc);          // first arrival: phase 0
+        bool ok = wait_bounded<false>(bar_tmem_alloc, 0, p.timeout_ns);
+        if (!ok)
+            record_error(kErrEpiTmemPhase0);
+        ptx::tcgen05_fence_after_thread_sync();
+        const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot);
+        ptx::griddep_wait();                       // C may belong to the previous kernel in the stream
+        if (ok && !wait_bounded<false>(bar_acc, 0, p.timeout_ns)) {
+            record_error(kErrEpiAccFull);
+            ok = false;
+        }
+        ptx::tcgen05_fence_after_thread_sync();
+        ok = __all_sync(0xffffffffu, ok);          // tcgen05.ld is warp-collective
+
+        float acc[M_PAD];
+        if (ok) {
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16);
+#pragma unroll
+            for (int j = 0; j < M_PAD / 8; ++j) {
+                uint32_t r[8];
+                ptx::tmem_ld_32x32b_x8(taddr + 8u * j, r);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[8 * j + i] = __uint_as_float(r[i]);
+            }
+            ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < M_PAD; ++i)
+                acc[i] = 0.0f;
+        }
+        if (p.probes != nullptr) {
+            unsigned long long t = ptx::globaltimer();
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+            if (lane == 0)
+                atomicMax(&p.probes[2 * blockIdx.x], t);
+        }
+        ptx::tcgen05_fence_before_thread_sync();
+        ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
+
+        int row;
+        const bool valid = tmem_row_of_thread(quarter, lane, row);   // row = n within the tile
+        if (SPLIT_K > 1 && rank != 0) {
+            // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
+            if (ok && valid && !p.drop_mailbox) {
+                const uint32_t dst = ptx::mapa_shared(
+                    sbase + L.mailbox + ((rank - 1u) * kTileN + (uint32_t)row) * (M_PAD * 4u), 0);
+                const uint32_t rbar = ptx::mapa_shared(bar_reduce, 0);
+#pragma unroll
+                for (int i = 0; i < M_PAD / 4; ++i)
+                    ptx::st_async_v4(dst + 16u * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+            }
+        } else {
+            if (SPLIT_K > 1) {
+                // Owner: relaxed cluster-scope observation of the mailbox phase,
+                // then one acquire fence restricted to shared::cluster memory.
+                if (!wait_bounded<true>(bar_reduce, 0, p.reduce_timeout_ns)) {
+                    record_error(kErrReduce);
+                    ok = false;
+                }
+                ptx::fence_acquire_shared_cluster();
+                if (valid && ok) {
+                    const float *box = reinterpret_cast<const float *>(smem + L.mailbox);
+#pragma unroll 1
+                    for (int r = 1; r < SPLIT_K; ++r) {            // fixed rank order
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(box + ((r - 1) * kTileN + row) * M_PAD);
+#pragma unroll
+                        for (int i = 0; i < M_PAD / 4; ++i) {
+                            const float4 v = src[i];
+                            acc[4 * i] += v.x;
+                            acc[4 * i + 1] += v.y;
+                            acc[4 * i + 2] += v.z;
+                            acc[4 * i + 3] += v.w;
+                        }
+                    }
+                }
+            }
+            __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
+            if (valid) {
+#pragma unroll
+                for (int m = 0; m < M_PAD; ++m)
+                    stage_out[m * kTileN + row] = __float2bfloat16_rn(acc[m]);
+                if (p.c_f32 != nullptr) {
+#pragma unroll
+                    for (int m = 0; m < M_PAD; ++m)
+                        if (m < p.M)
+                            p.c_f32[(size_t)m * p.N + n0 + row] = acc[m];
+                }
+            }
+            ptx::named_barrier_sync(1, kEpilogueThreads);
+            // 16-byte coalesced stores: row m of the tile is 64 bf16 = 8 chunks.
+            for (int c = etid; c < p.M * (kTileN / 8); c += kEpilogueThreads) {
+                const int m = c >> 3, ch = c & 7;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
+                *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
+            }
+        }
+    }
+}
+
+// The concurrent TMEM allocator of the stress method: allocate, fill with NaN,
+// free.  128 threads; never waits on another kernel.
+__global__ void __launch_bounds__(128) tmem_hog_kernel(int ncols, int iters)
+{
+    __shared__ uint32_t slot;
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(&slot), (uint32_t)ncols);
+        ptx::tmem_relinquish_alloc_permit();
+    }
+    ptx::tcgen05_fence_before_thread_sync();
+    __syncthreads();
+    ptx::tcgen05_fence_after_thread_sync();
+    const uint32_t base = slot + ((uint32_t)(32 * warp) << 16);
+    const uint32_t nan8[8] = {0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u,
+                              0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u};
+    for (int it = 0; it < iters; ++it)
+        for (int c = 0; c < ncols; c += 8)
+            ptx::tmem_st_32x32b_x8(base + (uint32_t)c, nan8);
+    ptx::tmem_wait_st();
+    ptx::tcgen05_fence_before_thread_sync();
+    __syncthreads();
+    ptx::tcgen05_fence_after_thread_sync();
+    if (warp == 0)
+        ptx::tmem_dealloc(slot, (uint32_t)ncols);
+}
+
+}  // namespace lowm

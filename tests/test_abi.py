@@ -1,0 +1,105 @@
+"""The C-ABI library builds, loads and exports what include/lowm_gemm.h declares.
+
+CPU-only: no call here touches a GPU.  Host-side argument checks that run
+before any device query (null and misaligned pointers, bad sizes) and the
+host-only tactic query are exercised directly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from split_bf16_gemm_swap_gb300 import build, lowm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lowm_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return lowm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(lowm_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_binding_functions():
+    assert tuple(declared_functions()) == lowm.ABI_FUNCTIONS
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert lowm.status_string(s)
+    assert "unknown" in lowm.status_string(99)
+
+
+def test_shipped_tactic_is_reproduced(L):
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK
+    assert (t["tile_n"], t["m_pad"], t["split_k"], t["block_k"]) == (64, 8, 2, 64)
+    assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["pdl"] == 1
+    assert t["stages"] >= 10 and t["smem_bytes"] <= 232448
+
+
+@pytest.mark.parametrize("M,N,K,sk,ctas", [(4, 2304, 12288, 4, 144), (4, 49152, 4096, 2, 1536),
+                                          (16, 6144, 32768, 4, 384), (64, 6144, 4096, 1, 96)])
+def test_cluster_counts_for_the_workloads(L, M, N, K, sk, ctas):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    assert st == lowm.LOWM_OK and t["ctas"] == ctas and t["split_k"] == sk
+    assert t["m_pad"] == (8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64)
+
+
+def test_auto_split_k_keeps_the_k_loop_non_empty(L):
+    for M, N, K in [(4, 64, 64), (4, 64, 128), (4, 6144, 4096), (64, 64, 512), (1, 49152, 4096)]:
+        st, t = lowm.lowm_gemm_query_tactic(M, N, K, 0)
+        assert st == lowm.LOWM_OK
+        assert K % (t["split_k"] * 64) == 0 and K // (t["split_k"] * 64) >= 1
+
+
+@pytest.mark.parametrize("M,N,K,sk,want", [
+    (0, 64, 64, 1, lowm.LOWM_ERR_INVALID_ARGUMENT),
+    (65, 64, 64, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),
+    (4, 96, 64, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # N not a multiple of 64
+    (4, 64, 96, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # K not a multiple of 64
+    (4, 64, 64, 2, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # empty K loop on one rank
+    (4, 64, 128, 3, lowm.LOWM_ERR_INVALID_ARGUMENT),      # split_k not a power of two
+    (4, 64, 1024, 16, lowm.LOWM_ERR_INVALID_ARGUMENT),
+    (4, -64, 64, 1, lowm.LOWM_ERR_INVALID_ARGUMENT),
+])
+def test_query_rejects_bad_shapes(L, M, N, K, sk, want):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    assert st == want and t is None
+
+
+def test_gemm_rejects_null_and_misaligned_pointers_before_touching_a_device(L):
+    assert lowm.lowm_gemm_bf16(0, 0x1000, 0x2000, 4, 64, 64, 1, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
+    assert lowm.lowm_gemm_bf16(0x1000, 0x2000, 0x3008, 4, 64, 64, 1, 0) == lowm.LOWM_ERR_MISALIGNED
+    assert lowm.lowm_gemm_bf16(0x1000, 0x2000, 0x3000, 0, 64, 64, 1, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
+    # C overlapping W
+    assert lowm.lowm_gemm_bf16(0x1000, 0x100000, 0x100040, 4, 64, 64, 1, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
+    assert lowm.lowm_gemm_bf16_debug(0x1000, 0x100000, 0x200000, 4, 64, 64, 1, 0, stages=1) \
+        == lowm.LOWM_ERR_INVALID_ARGUMENT
+    assert lowm.lowm_gemm_bf16_host(0, 1, 1, 1, 1, 1, 4, 64, 64, 0, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
+    assert lowm.lowm_tmem_hog_launch(0, 1, 48, 1) == lowm.LOWM_ERR_INVALID_ARGUMENT
+
+
+def test_library_does_not_reference_the_oracle():
+    src_dir = os.path.join(ROOT, "split_bf16_gemm_swap_gb300")
+    for dirpath, _, files in os.walk(src_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "oracle." not in text, f

@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bar (from the method's own check, "Fix two synchronization gaps in the
+MiniMax M3 low-M split-K GEMM", Hardware verification, which compares the bf16
+output with an fp32 product, and the exact-integer construction of
+"warpgroup_mma_wait does not properly synchronize across warpgroups"):
+  * integer-valued inputs: bit-exact, fp32 sums included;
+  * random inputs: the kernel's fp32 sums within 1e-5 * sqrt(K) * max|a| *
+    max|w| of the oracle's fp64 sums, the bf16 output exactly the
+    round-to-nearest-even of those fp32 sums, and within 1 bf16 ulp of the
+    oracle's single-rounded value wherever that bound is below a quarter ulp
+    (for outputs that cancel to a few ulps of the fp32 error, the absolute
+    bound is the bar, as it is for any fp32-accumulating GEMM);
+  * repeated launches: bitwise identical.
+Every case compares every output element.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_parity, f32_bound
+from split_bf16_gemm_swap_gb300 import build, inputs, lowm
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    lowm.lib()
+    torch.cuda.init()
+
+
+def sync_ok():
+    st, detail = lowm.lowm_gemm_sync_status()
+    assert st == lowm.LOWM_OK, "kernel status %d, bits %#x" % (st, detail)
+
+
+def run_gpu(A, W, split_k=0, want_f32=True, **dbg):
+    M, K = A.shape
+    N = W.shape[0]
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)   # unwritten outputs stay NaN
+    F = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV) if want_f32 else None
+    st = lowm.lowm_gemm_bf16_debug(Ad, Wd, C, M, N, K, split_k, None, c_f32=F, **dbg)
+    assert st == lowm.LOWM_OK, lowm.status_string(st)
+    sync_ok()
+    return inputs.bits(C.cpu()), (F.cpu().numpy().astype(np.float64) if F is not None else None)
+
+
+def check(A, W, split_k=0, exact=False):
+    M, K = A.shape
+    C, F = run_gpu(A, W, split_k)
+    Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+    if exact:
+        bad = np.argwhere(C != Cref)
+        assert bad.size == 0, "first mismatches (m, n): %s" % bad[:8].tolist()
+        assert np.array_equal(F, S)
+        return C
+    bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
+    assert_parity(C, F, Cref, S, bound)
+    return C
+
+
+# ---------------------------------------------------------------- small shapes
+SMALL = [
+    # M, N, K, split_k: several tiles, ragged M, ring wrap-around (K/64 > stages), every m_pad and split_k
+    (1, 64, 64, 1), (3, 192, 256, 1), (4, 640, 1024, 2), (5, 128, 512, 4), (8, 64, 1024, 8),
+    (7, 256, 4096, 1), (13, 256, 1024, 2), (16, 128, 2048, 4), (17, 192, 512, 1), (24, 128, 4096, 2),
+    (31, 64, 512, 2), (32, 320, 1024, 2), (33, 128, 256, 1), (48, 64, 1024, 4), (64, 192, 1024, 8),
+    (64, 128, 8192, 1), (2, 1024, 2048, 0), (9, 448, 3072, 0),
+]
+
+
+@pytest.mark.parametrize("M,N,K,split_k", SMALL)
+def test_small_shapes_random(M, N, K, split_k):
+    A, W = inputs.make_problem(M, N, K, seed=100 + M + N + K)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 128, 512, 1), (16, 192, 1024, 2), (64, 64, 2048, 4),
+                                           (3, 320, 4096, 8)])
+def test_small_shapes_integer_exact(M, N, K, split_k):
+    A, W = inputs.make_problem(M, N, K, seed=7, kind="int")
+    C = check(A, W, split_k, exact=True)
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(C, np.broadcast_to(inputs.bits(col[None, :]), C.shape))
+
+
+def test_identity_weight_maps_every_column():
+    # W[n, k] = 1 iff k == n: C[m, n] = A[m, n] exactly, so a wrong TMEM lane /
+    # column mapping or a transposed store shows up as a permutation.
+    M, N, K = 8, 64, 128
+    A = (torch.arange(M * K, dtype=torch.float32).reshape(M, K) % 251 + 1).to(torch.bfloat16)
+    W = torch.zeros((N, K), dtype=torch.bfloat16)
+    W[torch.arange(N), torch.arange(N)] = 1.0
+    for split_k in (1, 2):
+        C, _ = run_gpu(A, W, split_k, want_f32=False)
+        want = inputs.bits(A)[:, :N]
+        if not np.array_equal(C, want):
+            vals = {int(v): i for i, v in enumerate(want[0])}
+            got_cols = [vals.get(int(v), -1) for v in C[0]]
+            raise AssertionError("split_k %d: output column n holds input column %s" % (split_k, got_cols))
+
+
+def test_rows_beyond_M_are_not_written():
+    M, N, K = 3, 256, 512
+    A, W = inputs.make_problem(M, N, K, seed=3)
+    big = torch.full((M + 5, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    F = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    st = lowm.lowm_gemm_bf16_debug(A.to(DEV), W.to(DEV), big, M, N, K, 2, None, c_f32=F)
+    assert st == lowm.LOWM_OK
+    sync_ok()
+    assert torch.all(big[M:] == 7.0)
+    Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+    bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
+    assert_parity(inputs.bits(big[:M].cpu()), F.cpu().numpy().astype(np.float64), Cref, S, bound)
+
+
+# ---------------------------------------------------------------- the five workloads at full size
+def test_workload_m4_n6144_k4096_split2():
+    A, W = inputs.make_problem(4, 6144, 4096, seed=1234)
+    check(A, W, 2)
+
+
+def test_workload_m4_n2304_k12288_split4():
+    A, W = inputs.make_problem(4, 2304, 12288, seed=1234)
+    check(A, W, 4)
+
+
+def test_workload_m4_n49152_k4096_split2():
+    A, W = inputs.make_problem(4, 49152, 4096, seed=1234)
+    check(A, W, 2)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
+def test_workload_m_sweep_n6144_k4096(M):
+    A, W = inputs.make_problem(M, 6144, 4096, seed=1234)
+    st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 0)
+    assert st == lowm.LOWM_OK and t["split_k"] in (1, 2, 4)
+    check(A, W, 0)
+
+
+def test_workload_integer_m16_n6144_k32768_split4():
+    A, W = inputs.make_problem(16, 6144, 32768, seed=1234, kind="int")
+    C = check(A, W, 4, exact=True)
+    col = W.to(torch.int64).sum(dim=1)
+    assert int(col.abs().max()) < 2 ** 24
+    want = inputs.bits(col.to(torch.float32).to(torch.bfloat16)[None, :])
+    assert np.array_equal(C, np.broadcast_to(want, C.shape))
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (4, 2304, 12288, 4), (16, 6144, 32768, 4)])
+def test_twenty_launches_are_bitwise_identical(M, N, K, split_k):
+    A, W = inputs.make_problem(M, N, K, seed=99)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    outs = torch.empty((20, M, N), dtype=torch.bfloat16, device=DEV)
+    for i in range(20):
+        assert lowm.lowm_gemm_bf16(Ad, Wd, outs[i], M, N, K, split_k, None) == lowm.LOWM_OK
+    sync_ok()
+    o = outs.view(torch.int16)
+    assert bool((o == o[0:1]).all())
+
+
+def test_every_split_k_agrees_with_the_oracle():
+    A, W = inputs.make_problem(4, 1024, 8192, seed=5)
+    for sk in (1, 2, 4, 8):
+        check(A, W, sk)
+
+
+def test_pdl_chain_reads_the_previous_output():
+    # Each GEMM's A is the previous GEMM's C, launched back to back with PDL:
+    # griddepcontrol.wait must order the TMA reads of A after the producer's stores.
+    M, D = 4, 1024
+    A0, _ = inputs.make_problem(M, D, D, seed=11)
+    Ws = [inputs.make_problem(M, D, D, seed=20 + i)[1] for i in range(6)]
+    Wd = [w.to(DEV) for w in Ws]
+    Cs = [A0.to(DEV)] + [torch.empty((M, D), dtype=torch.bfloat16, device=DEV) for _ in Ws]
+    Fs = [torch.empty((M, D), dtype=torch.float32, device=DEV) for _ in Ws]
+    for i, w in enumerate(Wd):
+        assert lowm.lowm_gemm_bf16_debug(Cs[i], w, Cs[i + 1], M, D, D, 2, None, c_f32=Fs[i]) == lowm.LOWM_OK
+    sync_ok()
+    for i, w in enumerate(Ws):
+        a = Cs[i].cpu()
+        ref, S = oracle.gemm_bf16_f64(inputs.bits(a), inputs.bits(w))
+        bound = f32_bound(D, a.to(torch.float64).numpy(), w.to(torch.float64).numpy())
+        assert_parity(inputs.bits(Cs[i + 1].cpu()), Fs[i].cpu().numpy().astype(np.float64), ref, S, bound)
+
+
+def test_host_buffer_entry_point_matches_device_path():
+    M, N, K = 4, 6144, 4096
+    A, W = inputs.make_problem(M, N, K, seed=1234)
+    Ah, Wh = A.pin_memory(), W.pin_memory()
+    Ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    Ad = torch.empty_like(A, device=DEV)
+    Wd = torch.empty_like(W, device=DEV)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16_host(Ah, Wh, Ch, Ad, Wd, Cd, M, N, K, 2, None) == lowm.LOWM_OK
+    C_dev, _ = run_gpu(A, W, 2, want_f32=False)
+    assert np.array_equal(inputs.bits(Ch), C_dev)
+
+
+def test_full_capacity_request_gives_the_same_bits():
+    A, W = inputs.make_problem(4, 6144, 4096, seed=8)
+    C1, _ = run_gpu(A, W, 2, want_f32=False)
+    C2, _ = run_gpu(A, W, 2, want_f32=False, full_smem=1, stages=10)
+    assert np.array_equal(C1, C2)
+
+
+def test_a_dropped_mailbox_times_out_and_the_context_survives():
+    # Failure injection on the host side of the protocol: the non-owner ranks
+    # skip their publication, so the owner's bounded mailbox wait runs out.
+    A, W = inputs.make_problem(4, 256, 1024, seed=4)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    C = torch.empty((4, 256), dtype=torch.bfloat16, device=DEV)
+    st = lowm.lowm_gemm_bf16_debug(Ad, Wd, C, 4, 256, 1024, 2, None, drop_mailbox=1,
+                                   reduce_timeout_ns=20_000_000)
+    assert st == lowm.LOWM_OK
+    st, detail = lowm.lowm_gemm_sync_status()
+    assert st == lowm.LOWM_ERR_TIMEOUT and detail == (1 << 8), (st, hex(detail))
+    # the status word was cleared and the context still works
+    check(A, W, 2)

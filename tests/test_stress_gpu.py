@@ -1,0 +1,112 @@
+"""Race stress of the TMEM release ordering, on the GPU.
+
+The method of the TensorRT-LLM PR "Fix two synchronization gaps in the
+MiniMax M3 low-M split-K GEMM" (Hardware verification): stall two of the four
+epilogue warps before their first arrival on the TMEM barrier (5, 10 and
+100 us), keep the shared-memory request at the kernel's footprint so another
+kernel can co-reside on the SM, run a kernel on a second stream that
+allocates TMEM columns, fills them with NaN and frees them, and probe
+%globaltimer at the epilogue's tcgen05.ld and at the MMA warp's
+tcgen05.dealloc.  20 launches per configuration.
+
+Pass criteria: every stressed output is bitwise identical to the unstressed
+output (which is itself checked against the oracle / the closed form), no
+kernel wait times out, and in every CTA the dealloc timestamp is not earlier
+than the latest epilogue load.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_parity, f32_bound
+from split_bf16_gemm_swap_gb300 import build, inputs, lowm
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+LAUNCHES = 20
+STALL_WARPS = (1 << 4) | (1 << 5)          # two of the four epilogue warps (2..5)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    lowm.lib()
+
+
+def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK
+    ctas = t["ctas"]
+    s_gemm = torch.cuda.Stream()
+    s_hog = torch.cuda.Stream()
+    probes = torch.zeros((LAUNCHES, ctas, 2), dtype=torch.int64, device=DEV)
+    outs = torch.empty((LAUNCHES, M, N), dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+    for i in range(LAUNCHES):
+        for _ in range(3):
+            assert lowm.lowm_tmem_hog_launch(s_hog, 4096, hog_cols, 4) == lowm.LOWM_OK
+        st = lowm.lowm_gemm_bf16_debug(Ad, Wd, outs[i], M, N, K, split_k, s_gemm, stall_warp_mask=STALL_WARPS,
+                                       stall_rank_mask=stall_rank_mask, stall_ns=stall_ns, probes=probes[i])
+        assert st == lowm.LOWM_OK
+    torch.cuda.synchronize()
+    st, detail = lowm.lowm_gemm_sync_status(s_gemm)
+    assert st == lowm.LOWM_OK, "kernel wait timed out, bits %#x" % detail
+    return outs, probes.cpu().numpy()
+
+
+def check_probes(p):
+    t_ld, t_dealloc = p[..., 0], p[..., 1]
+    assert np.all(t_ld > 0) and np.all(t_dealloc > 0), "a CTA did not record both probes"
+    early = int(np.sum(t_dealloc < t_ld))
+    assert early == 0, "%d of %d CTAs freed TMEM before the epilogue's last load" % (early, t_ld.size)
+
+
+CONFIGS = [
+    # M, N, K, split_k, kind
+    (16, 6144, 32768, 4, "int"),
+    (4, 6144, 4096, 2, "randn"),
+    (4, 2304, 12288, 4, "randn"),
+    (4, 49152, 4096, 2, "randn"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,split_k,kind", CONFIGS)
+def test_stalled_epilogue_with_tmem_hog(M, N, K, split_k, kind):
+    A, W = inputs.make_problem(M, N, K, seed=1234, kind=kind)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    F = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    assert lowm.lowm_gemm_bf16_debug(Ad, Wd, ref, M, N, K, split_k, None, c_f32=F) == lowm.LOWM_OK
+    torch.cuda.synchronize()
+    ref_bits = inputs.bits(ref.cpu())
+    if kind == "int":
+        col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+        assert np.array_equal(ref_bits, np.broadcast_to(inputs.bits(col[None, :]), ref_bits.shape))
+    else:
+        Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+        bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
+        assert_parity(ref_bits, F.cpu().numpy().astype(np.float64), Cref, S, bound)
+    for stall_ns in (5_000, 10_000, 100_000):
+        outs, probes = stressed(Ad, Wd, M, N, K, split_k, stall_ns)
+        o = outs.view(torch.int16)
+        bad = int((o != ref.view(torch.int16)[None]).any(dim=2).any(dim=1).sum())
+        assert bad == 0, "stall %d ns: %d of %d launches differ from the unstressed output" % (
+            stall_ns, bad, LAUNCHES)
+        check_probes(probes)
+
+
+@pytest.mark.parametrize("stall_rank_mask", [1, 2])
+def test_stalling_only_one_rank(stall_rank_mask):
+    # The pages also stall only the owner or only the non-owner rank.
+    M, N, K, split_k = 4, 6144, 4096, 2
+    A, W = inputs.make_problem(M, N, K, seed=77)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16(Ad, Wd, ref, M, N, K, split_k, None) == lowm.LOWM_OK
+    outs, probes = stressed(Ad, Wd, M, N, K, split_k, 10_000, hog_cols=32, stall_rank_mask=stall_rank_mask)
+    assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
+    check_probes(probes)
