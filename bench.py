@@ -153,16 +153,33 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
 
 
+def max_over_ranks(x: float) -> float:
+    """Largest value of x over the ranks of the default process group (x itself without one)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(bytes_per_step: int, steps: int, world: int, secs_max: float) -> float:
+    """GB/s over all replicas: every rank did `steps` GEMMs; the job took the slowest rank's time."""
+    return world * bytes_per_step * steps / secs_max / 1e9
+
+
 # ------------------------------------------------------------------ our arm
 def build_graphs(lowm, A, Ws, C, w, stream, per_graph):
     """CUDA graphs of `per_graph` back-to-back launches, cycling through the W copies."""
     M, N, K, sk = w["M"], w["N"], w["K"], w["split_k"]
+    flags = w.get("flags", 0)
     graphs = []
     for g_i in range(len(Ws)):                      # graph g starts at W copy g: rotation continues across replays
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(per_graph):
-                st = lowm.lowm_gemm_bf16(A, Ws[(g_i * per_graph + i) % len(Ws)], C, M, N, K, sk, stream)
+                st = lowm.lowm_gemm_bf16_ex(A, Ws[(g_i * per_graph + i) % len(Ws)], C, M, N, K, sk, flags, stream)
                 if st != 0:
                     raise RuntimeError("lowm_gemm_bf16 failed during capture: %s" % lowm.status_string(st))
         graphs.append(g)
@@ -266,7 +283,7 @@ def run_ours(args):
         torch.distributed.barrier()
     from split_bf16_gemm_swap_gb300 import lowm
     lowm.lib()
-    w = dict(WORKLOAD)
+    w = dict(WORKLOAD, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT if args.w_before_pdl_wait else 0)
     st, tactic = lowm.lowm_gemm_query_tactic(w["M"], w["N"], w["K"], w["split_k"])
     assert st == 0, lowm.status_string(st)
     peak, peak_kind = measured_peak()
@@ -280,17 +297,16 @@ def run_ours(args):
         torch.cuda.synchronize(device)
         if world > 1:
             torch.distributed.barrier()
-    if world > 1:
-        t = torch.tensor([secs], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = float(t.item())
-    per_step = secs / args.steps
-    achieved = bytes_per / per_step / 1e9
-    value = world * bytes_per * args.steps / secs / 1e9
+    my_secs = secs
+    secs = max_over_ranks(secs)
+    per_step = my_secs / args.steps
+    achieved = bytes_per / per_step / 1e9                  # this rank's kernel, for the roofline
+    value = whole_job_rate(bytes_per, args.steps, world, secs)
 
     # wide-N line (same protocol, fewer steps)
     wide_steps = max(200, min(args.steps, 2000))
-    wsecs, _, wR = time_device(lowm, WIDE, wide_steps, max(args.warmup, 3), device)
+    wide_w = dict(WIDE, flags=w["flags"])
+    wsecs, _, wR = time_device(lowm, wide_w, wide_steps, max(args.warmup, 3), device)
     wbytes = algo_bytes(WIDE["M"], WIDE["N"], WIDE["K"])
     wide = {"workload": workload_name(WIDE), "us_per_gemm": wsecs / wide_steps * 1e6,
             "gbs": wbytes * wide_steps / wsecs / 1e9, "steps": wide_steps,
@@ -314,6 +330,8 @@ def run_ours(args):
                    "inputs": "A, W ~ N(0,1)/sqrt(K) rounded to bf16, seed 1234",
                    "l2": "inputs larger than L2: %d rotating W copies (%.0f MB)" % (R, R * w["N"] * w["K"] * 2 / 1e6),
                    "tactic": tactic, "launch": "CUDA graphs of 100 PDL launches, replayed",
+                   "entry_point": "lowm_gemm_bf16_ex(flags=%d)" % w["flags"],
+                   "w_before_pdl_wait": bool(w["flags"]),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
@@ -431,6 +449,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--w-before-pdl-wait", action="store_true",
+                    help="launch with LOWM_FLAG_W_BEFORE_PDL_WAIT (the W copies are never written by a kernel)")
     ap.add_argument("--profile-only", action="store_true",
                     help="plain launches of the workload for a profiler (no timing, no JSON line)")
     ap.add_argument("--wide", action="store_true", help="with --profile-only: the wide-N workload")

@@ -63,17 +63,30 @@ typedef enum {
  *                rows M..m_pad-1 are zero-filled by the TMA unit and never stored
  *   split_k      CTAs per cluster along K (1, 2, 4 or 8)
  *   stages       depth of the shared-memory ring between the TMA producer and the MMA warp
- *   block_k      K elements per ring stage (64: one 128-byte swizzle row of bf16)
- *   num_clusters N / tile_n
+ *   block_k      K elements per block (64: one 128-byte swizzle row of bf16)
+ *   tiles        N / tile_n output tiles
+ *   num_clusters clusters launched: `tiles` (one tile each), or fewer when
+ *                persistent
  *   ctas         num_clusters * split_k
  *   smem_bytes   dynamic shared memory requested per CTA
  *   pdl          1 when launched with programmatic dependent launch
+ *   persistent   1: each cluster walks tiles c, c + num_clusters, ... with a
+ *                continuous TMA stream and double-buffered accumulator,
+ *                mailbox and output staging (chosen when there are more tiles
+ *                than clusters that fit on the GPU at once; every cluster then
+ *                gets the same number of tiles, tiles_per_cluster)
+ *   tiles_per_cluster  ceil(tiles / num_clusters)
+ *   kb_per_stage 64-wide K blocks per ring stage, fetched by one 3-D TMA
+ *                copy of W and one of A (the largest of 4, 2, 1 dividing the
+ *                rank's block count): a copy has a fixed per-CTA cost, so
+ *                larger copies are what let one CTA stream its share of HBM
  * The pages' shipped tactic reads as (tile_n 64, m_pad 8, split_k 2, stages 10)
  * ("Fix two synchronization gaps ...", Hardware verification).
  */
 typedef struct {
     int tile_n, m_pad, split_k, stages, block_k;
-    int num_clusters, ctas, smem_bytes, pdl;
+    int tiles, num_clusters, ctas, smem_bytes, pdl;
+    int persistent, tiles_per_cluster, kb_per_stage;
 } lowm_tactic_t;
 
 /*
@@ -87,6 +100,25 @@ typedef struct {
  */
 lowm_status_t lowm_gemm_bf16(const void *A, const void *W, void *C,
                              int M, int N, int K, int split_k, void *stream);
+
+/*
+ * Flags for lowm_gemm_bf16_ex.
+ *
+ * LOWM_FLAG_W_BEFORE_PDL_WAIT: the caller promises that W is not written by
+ * the kernel that precedes this launch in the stream (true for weights).  The
+ * kernel may then request its first ring of W tiles before the programmatic
+ * dependent launch wait, so those loads overlap the preceding kernel's tail.
+ * A and C are still touched only after the wait.  Breaking the promise gives
+ * undefined results.
+ */
+#define LOWM_FLAG_W_BEFORE_PDL_WAIT 1u
+
+/*
+ * lowm_gemm_bf16 with launch flags (a bitwise OR of LOWM_FLAG_*; unknown bits
+ * are rejected with LOWM_ERR_INVALID_ARGUMENT).  flags == 0 is lowm_gemm_bf16.
+ */
+lowm_status_t lowm_gemm_bf16_ex(const void *A, const void *W, void *C,
+                                int M, int N, int K, int split_k, unsigned int flags, void *stream);
 
 /*
  * Fill *out with the tactic lowm_gemm_bf16 would launch for these arguments
@@ -147,6 +179,10 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
  *                    tcgen05.dealloc.  Zero-initialise before the launch.
  *   c_f32            NULL, or device float[M*N]: the fp32 sums before the bf16
  *                    rounding (written by the owner rank)
+ *   timeline         NULL, or device u64[4 * ctas]: per CTA, %globaltimer at
+ *                    [0] the end of the prologue, [1] the MMA warp's first
+ *                    full stage, [2] its last full stage, [3] the end of the
+ *                    epilogue (a diagnostic of where a launch spends its time)
  */
 typedef struct {
     unsigned int stall_warp_mask;
@@ -158,6 +194,7 @@ typedef struct {
     unsigned long long reduce_timeout_ns;
     unsigned long long *probes;
     float *c_f32;
+    unsigned long long *timeline;
 } lowm_debug_opts_t;
 
 /* lowm_gemm_bf16 with the hooks above (opts may be NULL: same as lowm_gemm_bf16). */

@@ -12,12 +12,14 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
 
 #include "../../include/lowm_gemm.h"
 #include "lowm_kernel.cuh"
+#include "lowm_persistent.cuh"
 
 namespace {
 
@@ -81,24 +83,44 @@ lowm_status_t check_device(int *sms_out)
 }
 
 // ------------------------------------------------------------------ tactics
+int env_int(const char *name, int dflt)
+{
+    const char *v = std::getenv(name);
+    return v && *v ? std::atoi(v) : dflt;
+}
+
 int m_pad_of(int M)
 {
     return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
 }
 
-int footprint(int m_pad, int split_k, int stages)
+int footprint(int m_pad, int split_k, int stages, int kbs, int bufs)
 {
-    return (int)lowm::make_smem_layout(m_pad, split_k, stages).bytes;
+    return (int)lowm::make_smem_layout(m_pad, split_k, stages, kbs, bufs).bytes;
 }
 
-// Deepest ring that lets `ctas_per_sm` CTAs share one SM.
-int stages_for(int m_pad, int split_k, int ctas_per_sm)
+// Deepest ring (at least 2 stages) that lets `ctas_per_sm` CTAs share one SM.
+int stages_for(int m_pad, int split_k, int kbs, int ctas_per_sm, int bufs)
 {
     const int budget = kSmemPerSm / ctas_per_sm - kSmemReservedPerCta;
     int s = 2;
-    while (s < 32 && footprint(m_pad, split_k, s + 1) <= budget && footprint(m_pad, split_k, s + 1) <= kMaxSmemPerCta)
+    while (s < 32 && footprint(m_pad, split_k, s + 1, kbs, bufs) <= budget &&
+           footprint(m_pad, split_k, s + 1, kbs, bufs) <= kMaxSmemPerCta)
         ++s;
     return s;
+}
+
+// K blocks per stage: the largest of 4, 2, 1 that divides the rank's block
+// count (LOWM_KB_PER_STAGE=1/2/4/8 overrides when it divides, for tuning).
+int choose_kb_per_stage(int kb_per_rank)
+{
+    const int force = env_int("LOWM_KB_PER_STAGE", 0);
+    if ((force == 1 || force == 2 || force == 4 || force == 8) && kb_per_rank % force == 0)
+        return force;
+    for (int b = 4; b > 1; b /= 2)
+        if (kb_per_rank % b == 0)
+            return b;
+    return 1;
 }
 
 bool shape_ok(int M, int N, int K, int split_k)
@@ -123,119 +145,35 @@ int choose_split_k(int M, int N, int K, int sms)
     return best;
 }
 
-lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, int stages_override, int full_smem,
-                          lowm_tactic_t *t)
-{
-    if (M <= 0 || N <= 0 || K <= 0 || split_k < 0)
-        return LOWM_ERR_INVALID_ARGUMENT;
-    if (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8)
-        return LOWM_ERR_INVALID_ARGUMENT;
-    if (split_k == 0)
-        split_k = choose_split_k(M, N, K, sms > 0 ? sms : 152);
-    if (split_k == 0 || !shape_ok(M, N, K, split_k))
-        return LOWM_ERR_UNSUPPORTED_SHAPE;
-    const int m_pad = m_pad_of(M);
-    // Two CTAs per SM by default: one CTA's prologue and epilogue overlap the
-    // other's stream, and the next kernel's CTAs (PDL) can start early.
-    int stages = stages_override > 0 ? stages_override : stages_for(m_pad, split_k, 2);
-    if (stages < 2)
-        return LOWM_ERR_INVALID_ARGUMENT;
-    const int fp = footprint(m_pad, split_k, stages);
-    if (fp > kMaxSmemPerCta)
-        return LOWM_ERR_UNSUPPORTED_SHAPE;
-    t->tile_n = lowm::kTileN;
-    t->m_pad = m_pad;
-    t->split_k = split_k;
-    t->stages = stages;
-    t->block_k = lowm::kBlockK;
-    t->num_clusters = N / lowm::kTileN;
-    t->ctas = t->num_clusters * split_k;
-    t->smem_bytes = full_smem ? kMaxSmemPerCta : fp;
-    t->pdl = 1;
-    return LOWM_OK;
-}
-
-// ------------------------------------------------------------------ TMA descriptors
-struct MapKey {
-    uintptr_t ptr;
-    int rows, K, box_rows;
-    bool operator==(const MapKey &o) const
-    {
-        return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows;
-    }
-};
-struct MapKeyHash {
-    size_t operator()(const MapKey &k) const
-    {
-        size_t h = std::hash<uintptr_t>()(k.ptr);
-        h ^= std::hash<long long>()(((long long)k.rows << 32) ^ ((long long)k.K << 8) ^ k.box_rows) + 0x9e3779b9 +
-             (h << 6) + (h >> 2);
-        return h;
-    }
-};
-std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;   // guarded by g_mu
-
-// 2-D map over a row-major [rows, K] bf16 matrix, box [box_rows, 64], 128-byte swizzle.
-lowm_status_t get_map(const void *ptr, int rows, int K, int box_rows, CUtensorMap *out)
-{
-    const MapKey key{reinterpret_cast<uintptr_t>(ptr), rows, K, box_rows};
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_maps.find(key);
-        if (it != g_maps.end()) {
-            *out = it->second;
-            return LOWM_OK;
-        }
-    }
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc)
-        return LOWM_ERR_CUDA;
-    CUtensorMap m;
-    std::memset(&m, 0, sizeof m);
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)lowm::kBlockK, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return LOWM_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_maps.size() > 4096)
-        g_maps.clear();
-    g_maps.emplace(key, m);
-    *out = m;
-    return LOWM_OK;
-}
-
-// ------------------------------------------------------------------ launch
+// ------------------------------------------------------------------ kernels
 typedef void (*KernelFn)(CUtensorMap, CUtensorMap, KernelParams);
 
 template <int MP, int SK>
-KernelFn kernel_ptr()
+KernelFn kernel_ptr(bool persistent)
 {
-    return reinterpret_cast<KernelFn>(&lowm::lowm_splitk_kernel<MP, SK>);
+    return persistent ? reinterpret_cast<KernelFn>(&lowm::lowm_splitk_persistent_kernel<MP, SK>)
+                      : reinterpret_cast<KernelFn>(&lowm::lowm_splitk_kernel<MP, SK>);
 }
 
 template <int MP>
-KernelFn kernel_for_split(int sk)
+KernelFn kernel_for_split(int sk, bool persistent)
 {
     switch (sk) {
-    case 1: return kernel_ptr<MP, 1>();
-    case 2: return kernel_ptr<MP, 2>();
-    case 4: return kernel_ptr<MP, 4>();
-    case 8: return kernel_ptr<MP, 8>();
+    case 1: return kernel_ptr<MP, 1>(persistent);
+    case 2: return kernel_ptr<MP, 2>(persistent);
+    case 4: return kernel_ptr<MP, 4>(persistent);
+    case 8: return kernel_ptr<MP, 8>(persistent);
     default: return nullptr;
     }
 }
 
-KernelFn kernel_for(int m_pad, int sk)
+KernelFn kernel_for(int m_pad, int sk, bool persistent)
 {
     switch (m_pad) {
-    case 8: return kernel_for_split<8>(sk);
-    case 16: return kernel_for_split<16>(sk);
-    case 32: return kernel_for_split<32>(sk);
-    case 64: return kernel_for_split<64>(sk);
+    case 8: return kernel_for_split<8>(sk, persistent);
+    case 16: return kernel_for_split<16>(sk, persistent);
+    case 32: return kernel_for_split<32>(sk, persistent);
+    case 64: return kernel_for_split<64>(sk, persistent);
     default: return nullptr;
     }
 }
@@ -259,6 +197,179 @@ lowm_status_t prepare_kernel(KernelFn fn)
     return LOWM_OK;
 }
 
+// Clusters of `split_k` CTAs that fit on the GPU at once with `smem` bytes
+// each: the occupancy API when a usable device is current, else the per-SM
+// arithmetic (shared memory and threads).
+int resident_clusters(int m_pad, int split_k, int smem, int sms, bool persistent, bool have_device)
+{
+    const int per_sm = std::min(kSmemPerSm / (smem + kSmemReservedPerCta), 2048 / lowm::kThreads);
+    const int formula = sms * per_sm / split_k;
+    if (!have_device)
+        return formula;
+    KernelFn fn = kernel_for(m_pad, split_k, persistent);
+    if (!fn || prepare_kernel(fn) != LOWM_OK)
+        return formula;
+    static std::mutex mu;
+    static std::unordered_map<long long, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const long long key = (((long long)reinterpret_cast<uintptr_t>(fn) * 64 + dev) * 262144) + smem;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end())
+            return it->second;
+    }
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(split_k * 1024), 1, 1);
+    cfg.blockDim = dim3(lowm::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)split_k;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(fn), &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = formula;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
+    return n;
+}
+
+lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_device, int stages_override,
+                          int full_smem, lowm_tactic_t *t)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || split_k < 0)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (split_k == 0)
+        split_k = choose_split_k(M, N, K, sms > 0 ? sms : 152);
+    if (split_k == 0 || !shape_ok(M, N, K, split_k))
+        return LOWM_ERR_UNSUPPORTED_SHAPE;
+    const int m_pad = m_pad_of(M);
+    const int tiles = N / lowm::kTileN;
+    int kbs = choose_kb_per_stage(K / (split_k * lowm::kBlockK));
+    while (kbs > 1 && footprint(m_pad, split_k, 2, kbs, 1) > kMaxSmemPerCta)
+        kbs /= 2;                                       // a 2-stage ring must fit
+    if (stages_override <= 0)
+        stages_override = env_int("LOWM_STAGES", 0);   // tuning hook: replaces the default ring depth
+    if (stages_override == 1)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    // Two CTAs per SM by default: one CTA's prologue and epilogue overlap the
+    // other's stream, and the next kernel's CTAs (PDL) can start early.
+    auto plan = [&](int bufs, int &stages, int &fp) {
+        stages = stages_override >= 2 ? stages_override : stages_for(m_pad, split_k, kbs, 2, bufs);
+        fp = footprint(m_pad, split_k, stages, kbs, bufs);
+    };
+    int stages = 0, fp = 0;
+    plan(1, stages, fp);
+    if (fp > kMaxSmemPerCta)
+        return LOWM_ERR_UNSUPPORTED_SHAPE;
+    int smem = full_smem ? kMaxSmemPerCta : fp;
+    // The persistent schedule is opt-in (LOWM_PERSISTENT=1) until it measures
+    // faster than one tile per cluster on the shapes it targets.
+    const bool persistent_wanted = env_int("LOWM_PERSISTENT", 0) == 1;
+    bool persistent = persistent_wanted;
+    int clusters = tiles;
+    if (persistent) {
+        int st2 = 0, fp2 = 0;
+        plan(2, st2, fp2);
+        if (fp2 <= kMaxSmemPerCta) {
+            stages = st2;
+            fp = fp2;
+            smem = full_smem ? kMaxSmemPerCta : fp;
+            int fit = std::max(1, resident_clusters(m_pad, split_k, smem, sms, true, have_device));
+            const int cap = env_int("LOWM_MAX_CLUSTERS", 0);   // tuning / test hook: fewer clusters
+            if (cap > 0)
+                fit = std::min(fit, cap);
+            const int per = (tiles + std::min(tiles, fit) - 1) / std::min(tiles, fit);
+            clusters = (tiles + per - 1) / per;          // every cluster gets `per` tiles (the last maybe fewer)
+        } else {
+            persistent = false;
+        }
+    }
+    t->tile_n = lowm::kTileN;
+    t->m_pad = m_pad;
+    t->split_k = split_k;
+    t->stages = stages;
+    t->block_k = lowm::kBlockK;
+    t->tiles = tiles;
+    t->num_clusters = clusters;
+    t->ctas = clusters * split_k;
+    t->smem_bytes = smem;
+    t->pdl = 1;
+    t->persistent = persistent ? 1 : 0;
+    t->tiles_per_cluster = (tiles + clusters - 1) / clusters;
+    t->kb_per_stage = kbs;
+    return LOWM_OK;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+struct MapKey {
+    uintptr_t ptr;
+    int rows, K, box_rows, box_kb;
+    bool operator==(const MapKey &o) const
+    {
+        return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && box_kb == o.box_kb;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        size_t h = std::hash<uintptr_t>()(k.ptr);
+        h ^= std::hash<long long>()(((long long)k.rows << 32) ^ ((long long)k.K << 12) ^ (k.box_rows << 4) ^
+                                    k.box_kb) +
+             0x9e3779b9 + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;   // guarded by g_mu
+
+// 3-D view (k_inner, row, k_block) of a row-major [rows, K] bf16 matrix:
+// extents {64, rows, K / 64}, byte strides {2K (row), 128 (k block)}.  A box
+// {64, box_rows, box_kb} lands in shared memory as box_kb consecutive
+// [box_rows x 64] tiles with 128-byte swizzling, the layout the MMA
+// descriptors expect.  Rows beyond `rows` are zero-filled.
+lowm_status_t get_map(const void *ptr, int rows, int K, int box_rows, int box_kb, CUtensorMap *out)
+{
+    const MapKey key{reinterpret_cast<uintptr_t>(ptr), rows, K, box_rows, box_kb};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return LOWM_OK;
+        }
+    }
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc)
+        return LOWM_ERR_CUDA;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[3] = {(cuuint64_t)lowm::kBlockK, (cuuint64_t)rows, (cuuint64_t)(K / lowm::kBlockK)};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)lowm::kBlockK * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)lowm::kBlockK, (cuuint32_t)box_rows, (cuuint32_t)box_kb};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return LOWM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_maps.size() > 4096)
+        g_maps.clear();
+    g_maps.emplace(key, m);
+    *out = m;
+    return LOWM_OK;
+}
+
+// ------------------------------------------------------------------ launch
 bool aligned16(const void *p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -271,8 +382,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 }
 
 lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K, int split_k, void *stream,
-                     const lowm_debug_opts_t *dbg)
+                     const lowm_debug_opts_t *dbg, unsigned int flags = 0)
 {
+    if (flags & ~LOWM_FLAG_W_BEFORE_PDL_WAIT)
+        return LOWM_ERR_INVALID_ARGUMENT;
     if (!A || !W || !C)
         return LOWM_ERR_INVALID_ARGUMENT;
     if (M <= 0 || N <= 0 || K <= 0)
@@ -289,18 +402,18 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     if (st != LOWM_OK)
         return st;
     lowm_tactic_t t;
-    st = make_tactic(M, N, K, split_k, sms, dbg ? dbg->stages : 0, (dbg && dbg->full_smem) ? 1 : 0, &t);
+    st = make_tactic(M, N, K, split_k, sms, true, dbg ? dbg->stages : 0, (dbg && dbg->full_smem) ? 1 : 0, &t);
     if (st != LOWM_OK)
         return st;
-    KernelFn fn = kernel_for(t.m_pad, t.split_k);
+    KernelFn fn = kernel_for(t.m_pad, t.split_k, t.persistent != 0);
     if (!fn)
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     if ((st = prepare_kernel(fn)) != LOWM_OK)
         return st;
     CUtensorMap map_a, map_w;
-    if ((st = get_map(A, M, K, t.m_pad, &map_a)) != LOWM_OK)
+    if ((st = get_map(A, M, K, t.m_pad, t.kb_per_stage, &map_a)) != LOWM_OK)
         return st;
-    if ((st = get_map(W, N, K, lowm::kTileN, &map_w)) != LOWM_OK)
+    if ((st = get_map(W, N, K, lowm::kTileN, t.kb_per_stage, &map_w)) != LOWM_OK)
         return st;
 
     KernelParams p;
@@ -311,8 +424,11 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     p.K = K;
     p.stages = t.stages;
     p.kb_per_rank = K / (t.split_k * lowm::kBlockK);
+    p.kb_per_stage = t.kb_per_stage;
+    p.num_tiles = t.tiles;
     p.timeout_ns = lowm::kDefaultTimeoutNs;
     p.reduce_timeout_ns = lowm::kDefaultTimeoutNs;
+    p.w_before_pdl_wait = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) ? 1u : 0u;
     if (dbg) {
         p.stall_warp_mask = dbg->stall_warp_mask;
         p.stall_rank_mask = dbg->stall_rank_mask;
@@ -320,6 +436,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
         p.drop_mailbox = dbg->drop_mailbox ? 1u : 0u;
         p.probes = dbg->probes;
         p.c_f32 = dbg->c_f32;
+        p.timeline = dbg->timeline;
         if (dbg->reduce_timeout_ns)
             p.reduce_timeout_ns = dbg->reduce_timeout_ns;
     }
@@ -345,8 +462,11 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
     if (std::getenv("LOWM_LOG"))
-        std::fprintf(stderr, "lowm: M%d N%d K%d -> tile_n %d m_pad %d split_k %d stages %d ctas %d smem %d\n", M, N,
-                     K, t.tile_n, t.m_pad, t.split_k, t.stages, t.ctas, t.smem_bytes);
+        std::fprintf(stderr,
+                     "lowm: M%d N%d K%d -> tile_n %d m_pad %d split_k %d stages %d x %d blocks ctas %d smem %d "
+                     "persistent %d\n",
+                     M, N, K, t.tile_n, t.m_pad, t.split_k, t.stages, t.kb_per_stage, t.ctas, t.smem_bytes,
+                     t.persistent);
     if (cudaLaunchKernelEx(&cfg, fn, map_a, map_w, p) != cudaSuccess)
         return LOWM_ERR_CUDA;
     return LOWM_OK;
@@ -361,6 +481,12 @@ lowm_status_t lowm_gemm_bf16(const void *A, const void *W, void *C, int M, int N
     return launch(A, W, C, M, N, K, split_k, stream, nullptr);
 }
 
+lowm_status_t lowm_gemm_bf16_ex(const void *A, const void *W, void *C, int M, int N, int K, int split_k,
+                                unsigned int flags, void *stream)
+{
+    return launch(A, W, C, M, N, K, split_k, stream, nullptr, flags);
+}
+
 lowm_status_t lowm_gemm_bf16_debug(const void *A, const void *W, void *C, int M, int N, int K, int split_k,
                                    void *stream, const lowm_debug_opts_t *opts)
 {
@@ -371,14 +497,19 @@ lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tact
 {
     if (!out)
         return LOWM_ERR_INVALID_ARGUMENT;
-    int sms = 152;   // host-only query: use the device's count when one is current and usable
-    int dev = 0, n = 0;
-    if (cudaGetDeviceCount(&n) == cudaSuccess && n > 0 && cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    else
+    // Host-only query: with a usable sm_103 device current, the same numbers the
+    // launch uses; otherwise the per-SM arithmetic for a 152-SM GB300.
+    int sms = 152;
+    int n = 0;
+    bool have_device = false;
+    if (cudaGetDeviceCount(&n) == cudaSuccess && n > 0)
+        have_device = check_device(&sms) == LOWM_OK;
+    if (!have_device) {
         cudaGetLastError();
+        sms = 152;
+    }
     lowm_tactic_t t;
-    const lowm_status_t st = make_tactic(M, N, K, split_k, sms, 0, 0, &t);
+    const lowm_status_t st = make_tactic(M, N, K, split_k, sms, have_device, 0, 0, &t);
     if (st == LOWM_OK)
         *out = t;
     return st;
@@ -425,7 +556,7 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
     lowm_status_t st = check_device(&sms);
     if (st != LOWM_OK)
         return st;
-    if ((st = make_tactic(M, N, K, split_k, sms, 0, 0, &t)) != LOWM_OK)
+    if ((st = make_tactic(M, N, K, split_k, sms, true, 0, 0, &t)) != LOWM_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(A_dev, A_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||

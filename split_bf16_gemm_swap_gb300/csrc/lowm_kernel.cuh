@@ -3,9 +3,14 @@
 // One CTA owns a 64-column slice of C (tile_n = 64) and 1/split_k of K.  The
 // split_k CTAs of a slice form one thread-block cluster along grid x; rank 0
 // of the cluster is the owner that reduces and stores.  Warp roles:
-//   warp 0      TMA producer: streams W tiles [64 n x 64 k] and A tiles
-//               [m_pad x 64 k] into a ring of `stages` shared-memory stages
-//               (full/empty mbarrier pair per stage).
+//   warp 0      TMA producer: streams W and A through a ring of `stages`
+//               shared-memory stages (full/empty mbarrier pair per stage).
+//               A stage holds `kb_per_stage` 64-wide K blocks: one 3-D copy of
+//               W [kb_per_stage x 64 n x 64 k] and one of A [kb_per_stage x
+//               m_pad x 64 k], each block a standard 128-byte-swizzled tile.
+//               A copy costs about the same fixed time per CTA whatever its
+//               size, so fewer, larger copies are what lets one CTA stream
+//               its share of HBM bandwidth.
 //   warp 1      MMA warp: allocates TMEM, issues tcgen05.mma (swap-AB: the W
 //               tile is the MMA's A operand with M = 64, the activation tile
 //               is its B operand with N = m_pad), releases each stage with
@@ -40,12 +45,13 @@
 namespace lowm {
 
 constexpr int kTileN = 64;          // output columns per CTA = MMA M
-constexpr int kBlockK = 64;         // K elements per ring stage (one 128-byte swizzle row)
+constexpr int kBlockK = 64;         // K elements per block (one 128-byte swizzle row of bf16)
 constexpr int kMmaK = 16;           // K per tcgen05.mma of kind::f16
+constexpr int kMaxKbPerStage = 8;   // K blocks per stage: 1, 2, 4 or 8
 constexpr int kThreads = 192;       // 6 warps
 constexpr int kEpilogueWarp0 = 2;   // warps 2..5; warp % 4 covers every TMEM lane quarter once
 constexpr int kEpilogueThreads = 128;
-constexpr uint32_t kWStageBytes = kTileN * kBlockK * 2;   // 8 KiB
+constexpr uint32_t kWBlockBytes = kTileN * kBlockK * 2;   // 8 KiB per 64 x 64 W block
 constexpr uint32_t kTmemBarArrivals = 32 + kEpilogueThreads;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;     // 2 s per wait on another party
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;       // 2 s for this CTA's own copies / MMAs in flight
@@ -68,15 +74,19 @@ __device__ unsigned int g_lowm_status;   // read and cleared by lowm_gemm_sync_s
 struct KernelParams {
     __nv_bfloat16 *C;
     int M, N, K;
-    int stages;
+    int stages;             // ring depth
+    int kb_per_stage;       // 64-wide K blocks per stage (divides kb_per_rank)
     int kb_per_rank;        // 64-wide K blocks per cluster rank
+    int num_tiles;          // N / 64 (the persistent kernel walks them; the other kernel has one per cluster)
     uint64_t timeout_ns;    // bound on every wait for another party
     uint64_t reduce_timeout_ns;   // bound on the owner's mailbox wait
     // test hooks
     uint32_t stall_warp_mask, stall_rank_mask, stall_ns;
     uint32_t drop_mailbox;  // non-owner ranks skip their publication (the owner's wait runs out)
+    uint32_t w_before_pdl_wait;   // caller's promise: the preceding kernel does not write W
     unsigned long long *probes;
     float *c_f32;
+    unsigned long long *timeline;   // [4 * ctas]: prologue end, first / last full stage, epilogue end
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).  The same
@@ -85,20 +95,23 @@ struct SmemLayout {
     uint32_t w, a, mailbox, out, bars, tmem_slot, bytes;
 };
 
-__host__ __device__ inline SmemLayout make_smem_layout(int m_pad, int split_k, int stages)
+// `bufs` = 1 for the one-tile-per-cluster kernel, 2 for the persistent kernel
+// (double-buffered mailbox and output staging).
+__host__ __device__ inline SmemLayout make_smem_layout(int m_pad, int split_k, int stages, int kb_per_stage,
+                                                       int bufs = 1)
 {
     SmemLayout L;
     uint32_t off = 0;
-    L.w = off;
-    off += (uint32_t)stages * kWStageBytes;
-    L.a = off;                                            // m_pad * 128 is a multiple of 1024
-    off += (uint32_t)stages * (uint32_t)m_pad * 128u;
-    L.mailbox = off;                                      // [(split_k-1)][64 n][m_pad] fp32
-    off += (uint32_t)(split_k - 1) * kTileN * (uint32_t)m_pad * 4u;
-    L.out = off;                                          // [m_pad][64 n] bf16 staging for C
-    off += (uint32_t)m_pad * kTileN * 2u;
-    L.bars = off;                                         // full[stages], empty[stages], acc, tmem, reduce
-    off += (uint32_t)(2 * stages + 3) * 8u;
+    L.w = off;                                            // [stages][kb_per_stage][64 n][64 k] bf16
+    off += (uint32_t)stages * (uint32_t)kb_per_stage * kWBlockBytes;
+    L.a = off;                                            // [stages][kb_per_stage][m_pad][64 k]; m_pad*128 % 1024 == 0
+    off += (uint32_t)stages * (uint32_t)kb_per_stage * (uint32_t)m_pad * 128u;
+    L.mailbox = off;                                      // [bufs][(split_k-1)][64 n][m_pad] fp32
+    off += (uint32_t)bufs * (uint32_t)(split_k - 1) * kTileN * (uint32_t)m_pad * 4u;
+    L.out = off;                                          // [bufs][m_pad][64 n] bf16 staging for C
+    off += (uint32_t)bufs * (uint32_t)m_pad * kTileN * 2u;
+    L.bars = off;                                         // full[stages], empty[stages], then per-kernel barriers
+    off += (uint32_t)(2 * stages + 12) * 8u;
     L.tmem_slot = off;
     off += 16;
     L.bytes = off + 1024;                                 // slack to align the dynamic base
@@ -132,6 +145,11 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int mma_m, int mma_n)
            | ((uint32_t)(mma_m >> 4) << 24);              // M >> 4
 }
 
+__host__ __device__ constexpr uint32_t tmem_cols_for(int cols)
+{
+    return cols <= 32 ? 32u : (cols <= 64 ? 64u : (cols <= 128 ? 128u : (cols <= 256 ? 256u : 512u)));
+}
+
 // TMEM placement of the M = 64 (cta_group::1) accumulator: row i of D lives
 // in lane 32 * (i / 16) + i % 16, i.e. the first 16 lanes of each 32-lane
 // quarter.  An epilogue warp with quarter q therefore holds rows 16q..16q+15
@@ -140,6 +158,38 @@ __device__ __forceinline__ bool tmem_row_of_thread(int quarter, int lane, int &r
 {
     row = 16 * quarter + lane;
     return lane < 16;
+}
+
+// Epilogue load of this warp's lane quarter: M_PAD fp32 columns, then
+// tcgen05.wait::ld.
+template <int M_PAD>
+__device__ __forceinline__ void load_accumulator(uint32_t taddr, float (&acc)[M_PAD])
+{
+#pragma unroll
+    for (int q = 0; q < M_PAD / 8; ++q) {
+        uint32_t r[8];
+        ptx::tmem_ld_32x32b_x8(taddr + 8u * q, r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[8 * q + i] = __uint_as_float(r[i]);
+    }
+    ptx::tmem_wait_ld();
+}
+
+// One stage's MMAs: kb_per_stage blocks x 4 K16 steps into the accumulator at
+// tmem_d.  `first` clears the accumulator with the stage's first MMA.
+template <int M_PAD>
+__device__ __forceinline__ void mma_stage(uint32_t tmem_d, uint32_t w_stage, uint32_t a_stage, int kb_per_stage,
+                                          bool first)
+{
+    constexpr uint32_t kIdesc = make_idesc_bf16(kTileN, M_PAD);
+    for (int j = 0; j < kb_per_stage; ++j) {
+        const uint64_t adesc = make_sw128_kmajor_desc(w_stage + (uint32_t)j * kWBlockBytes);
+        const uint64_t bdesc = make_sw128_kmajor_desc(a_stage + (uint32_t)j * (M_PAD * 128u));
+#pragma unroll
+        for (int kk = 0; kk < kBlockK / kMmaK; ++kk)      // +32 bytes of K per step: +2 in the encoded address
+            ptx::mma_bf16_ss(tmem_d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (first && j == 0 && kk == 0) ? 0u : 1u);
+    }
 }
 
 template <bool kClusterScope>
@@ -172,17 +222,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     static_assert(M_PAD % 8 == 0 && M_PAD >= 8 && M_PAD <= 64, "m_pad is the MMA N: 8..64 in steps of 8");
     static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
-    constexpr uint32_t kAStageBytes = M_PAD * 128u;
-    constexpr uint32_t kStageTx = kWStageBytes + kAStageBytes;
-    constexpr uint32_t kTmemCols = M_PAD <= 32 ? 32u : 64u;
+    constexpr uint32_t kTmemCols = tmem_cols_for(M_PAD);
     constexpr uint32_t kSlotBytes = kTileN * M_PAD * 4u;          // one rank's fp32 partial tile
-    constexpr uint32_t kIdesc = make_idesc_bf16(kTileN, M_PAD);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout L = make_smem_layout(M_PAD, SPLIT_K, p.stages);
+    const int kbs = p.kb_per_stage;
+    const SmemLayout L = make_smem_layout(M_PAD, SPLIT_K, p.stages, kbs);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int stages = p.stages;
+    const uint32_t w_stage_bytes = (uint32_t)kbs * kWBlockBytes;
+    const uint32_t a_stage_bytes = (uint32_t)kbs * (M_PAD * 128u);
+    const uint32_t stage_tx = w_stage_bytes + a_stage_bytes;
+    const int n_stages = p.kb_per_rank / kbs;                     // stage iterations of this rank
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = SPLIT_K > 1 ? ptx::cluster_ctarank() : 0u;
@@ -220,25 +272,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         __syncthreads();
     }
+    if (p.timeline != nullptr && threadIdx.x == 0)
+        p.timeline[4 * blockIdx.x] = ptx::globaltimer();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            ptx::griddep_wait();          // A (and C) may belong to the previous kernel in the stream
             const uint64_t pol_w = ptx::policy_evict_first();   // W is streamed once
             const uint64_t pol_a = ptx::policy_evict_last();    // A is re-read by every CTA
-            int issued = 0;
-            for (int kb = 0; kb < p.kb_per_rank; ++kb) {
-                const int s = kb % stages;
-                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+            // With the caller's promise that W is not written by the preceding
+            // kernel, the first ring of W is requested before the
+            // programmatic-dependency wait, overlapping that kernel's tail.  A
+            // (and C, in the epilogue) are touched only after the wait.
+            const int pre = p.w_before_pdl_wait ? (n_stages < stages ? n_stages : stages) : 0;
+            for (int i = 0; i < pre; ++i) {            // fresh ring: these stages are free
+                ptx::mbar_arrive_expect_tx(bar_full + 8u * i, stage_tx);
+                ptx::tma_load_3d(sbase + L.w + (uint32_t)i * w_stage_bytes, &tmap_w, 0, n0, kb0 + i * kbs,
+                                 bar_full + 8u * i, pol_w);
+            }
+            ptx::griddep_wait();          // A (and C) may belong to the previous kernel in the stream
+            for (int i = 0; i < pre; ++i)
+                ptx::tma_load_3d(sbase + L.a + (uint32_t)i * a_stage_bytes, &tmap_a, 0, 0, kb0 + i * kbs,
+                                 bar_full + 8u * i, pol_a);
+            int issued = pre;
+            for (int i = pre; i < n_stages; ++i) {
+                const int s = i % stages;
+                const uint32_t ph = (uint32_t)(i / stages) & 1u;
                 if (!wait_bounded<false>(bar_empty + 8u * s, ph ^ 1u, p.timeout_ns)) {
                     record_error(kErrProducerEmpty);
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(bar_full + 8u * s, kStageTx);
-                const int kx = (kb0 + kb) * kBlockK;
-                ptx::tma_load_2d(sbase + L.w + (uint32_t)s * kWStageBytes, &tmap_w, kx, n0, bar_full + 8u * s, pol_w);
-                ptx::tma_load_2d(sbase + L.a + (uint32_t)s * kAStageBytes, &tmap_a, kx, 0, bar_full + 8u * s, pol_a);
+                ptx::mbar_arrive_expect_tx(bar_full + 8u * s, stage_tx);
+                const int kz = kb0 + i * kbs;
+                ptx::tma_load_3d(sbase + L.w + (uint32_t)s * w_stage_bytes, &tmap_w, 0, n0, kz, bar_full + 8u * s,
+                                 pol_w);
+                ptx::tma_load_3d(sbase + L.a + (uint32_t)s * a_stage_bytes, &tmap_a, 0, 0, kz, bar_full + 8u * s,
+                                 pol_a);
                 ++issued;
             }
             ptx::griddep_launch_dependents();
@@ -262,19 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar_tmem_alloc);          // phase 0: "TMEM allocated" (32 lanes)
 
         if (lane == 0) {
-            for (int kb = 0; kb < p.kb_per_rank; ++kb) {
-                const int s = kb % stages;
-                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+            for (int i = 0; i < n_stages; ++i) {
+                const int s = i % stages;
+                const uint32_t ph = (uint32_t)(i / stages) & 1u;
                 if (!wait_bounded<false>(bar_full + 8u * s, ph, p.timeout_ns)) {
                     record_error(kErrMmaFull);
                     break;
                 }
+                if (p.timeline != nullptr && (i == 0 || i == n_stages - 1))
+                    p.timeline[4 * blockIdx.x + (i == 0 ? 1 : 2)] = ptx::globaltimer();
                 ptx::tcgen05_fence_after_thread_sync();
-                const uint64_t adesc = make_sw128_kmajor_desc(sbase + L.w + (uint32_t)s * kWStageBytes);
-                const uint64_t bdesc = make_sw128_kmajor_desc(sbase + L.a + (uint32_t)s * kAStageBytes);
-#pragma unroll
-                for (int kk = 0; kk < kBlockK / kMmaK; ++kk)      // +32 bytes of K per step: +2 in the encoded address
-                    ptx::mma_bf16_ss(tmem_d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kb | kk) != 0);
+                mma_stage<M_PAD>(tmem_d, sbase + L.w + (uint32_t)s * w_stage_bytes,
+                                 sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, i == 0);
                 ptx::tcgen05_commit(bar_empty + 8u * s);           // stage free once these MMAs have read it
             }
             ptx::tcgen05_commit(bar_acc);                          // accumulator complete
@@ -333,16 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float acc[M_PAD];
         if (ok) {
-            const uint32_t taddr = tmem_base + ((uint32_t)(32 * quarter) << 16);
-#pragma unroll
-            for (int j = 0; j < M_PAD / 8; ++j) {
-                uint32_t r[8];
-                ptx::tmem_ld_32x32b_x8(taddr + 8u * j, r);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[8 * j + i] = __uint_as_float(r[i]);
-            }
-            ptx::tmem_wait_ld();
+            load_accumulator<M_PAD>(tmem_base + ((uint32_t)(32 * quarter) << 16), acc);
         } else {
 #pragma unroll
             for (int i = 0; i < M_PAD; ++i)
@@ -371,6 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < M_PAD / 4; ++i)
                     ptx::st_async_v4(dst + 16u * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
             }
+            if (p.timeline != nullptr && etid == 0)
+                p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
         } else {
             if (SPLIT_K > 1) {
                 // Owner: relaxed cluster-scope observation of the mailbox phase,
@@ -416,6 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
                 *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
             }
+            if (p.timeline != nullptr && etid == 0)
+                p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
         }
     }
 }

@@ -68,6 +68,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Arrive on an mbarrier in another CTA of the cluster (shared::cluster
+// address from mapa_shared), releasing this thread's prior accesses at
+// cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote_release_cluster(uint32_t remote_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
 // Default semantics: .acquire at .cta scope.  Right for barriers completed by
 // this CTA's own threads, its TMA unit or its tensor-core commits.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
@@ -187,6 +195,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// 3-D tiled bulk tensor load (coordinates x innermost), same completion
+// mechanism.  Used with the (k_inner, row, k_block) view of a row-major
+// matrix, so one copy brings several 64-wide K blocks of a row slab.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
 }
 

@@ -23,9 +23,12 @@ LOWM_ERR_UNSUPPORTED_ARCH = 4
 LOWM_ERR_CUDA = 5
 LOWM_ERR_TIMEOUT = 6
 
+LOWM_FLAG_W_BEFORE_PDL_WAIT = 1
+
 # Exported C functions, in header order.
 ABI_FUNCTIONS = (
     "lowm_gemm_bf16",
+    "lowm_gemm_bf16_ex",
     "lowm_gemm_query_tactic",
     "lowm_status_string",
     "lowm_gemm_sync_status",
@@ -37,7 +40,8 @@ ABI_FUNCTIONS = (
 
 class lowm_tactic_t(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in
-                ("tile_n", "m_pad", "split_k", "stages", "block_k", "num_clusters", "ctas", "smem_bytes", "pdl")]
+                ("tile_n", "m_pad", "split_k", "stages", "block_k", "tiles", "num_clusters", "ctas", "smem_bytes",
+                 "pdl", "persistent", "tiles_per_cluster", "kb_per_stage")]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -54,6 +58,7 @@ class lowm_debug_opts_t(ctypes.Structure):
         ("reduce_timeout_ns", ctypes.c_ulonglong),
         ("probes", ctypes.c_void_p),
         ("c_f32", ctypes.c_void_p),
+        ("timeline", ctypes.c_void_p),
     ]
 
 
@@ -77,6 +82,8 @@ def lib():
         vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
         L.lowm_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, vp]
         L.lowm_gemm_bf16.restype = st
+        L.lowm_gemm_bf16_ex.argtypes = [vp, vp, vp, i, i, i, i, ctypes.c_uint, vp]
+        L.lowm_gemm_bf16_ex.restype = st
         L.lowm_gemm_query_tactic.argtypes = [i, i, i, i, ctypes.POINTER(lowm_tactic_t)]
         L.lowm_gemm_query_tactic.restype = st
         L.lowm_status_string.argtypes = [st]
@@ -122,6 +129,11 @@ def lowm_gemm_bf16(A, W, C, M: int, N: int, K: int, split_k: int = 0, stream=Non
     return lib().lowm_gemm_bf16(_ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K), int(split_k), _stream(stream))
 
 
+def lowm_gemm_bf16_ex(A, W, C, M: int, N: int, K: int, split_k: int = 0, flags: int = 0, stream=None) -> int:
+    return lib().lowm_gemm_bf16_ex(_ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K), int(split_k), int(flags),
+                                   _stream(stream))
+
+
 def lowm_gemm_query_tactic(M: int, N: int, K: int, split_k: int = 0):
     """Return ``(status, tactic dict or None)``."""
     t = lowm_tactic_t()
@@ -143,9 +155,9 @@ def lowm_gemm_bf16_host(A_host, W_host, C_host, A_dev, W_dev, C_dev, M, N, K, sp
 
 def lowm_gemm_bf16_debug(A, W, C, M, N, K, split_k=0, stream=None, *, stall_warp_mask=0, stall_rank_mask=0,
                          stall_ns=0, full_smem=0, stages=0, drop_mailbox=0, reduce_timeout_ns=0, probes=None,
-                         c_f32=None) -> int:
+                         c_f32=None, timeline=None) -> int:
     o = lowm_debug_opts_t(int(stall_warp_mask), int(stall_rank_mask), int(stall_ns), int(full_smem), int(stages),
-                          int(drop_mailbox), int(reduce_timeout_ns), _ptr(probes), _ptr(c_f32))
+                          int(drop_mailbox), int(reduce_timeout_ns), _ptr(probes), _ptr(c_f32), _ptr(timeline))
     return lib().lowm_gemm_bf16_debug(_ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K), int(split_k),
                                       _stream(stream), ctypes.byref(o))
 

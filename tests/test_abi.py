@@ -50,16 +50,54 @@ def test_shipped_tactic_is_reproduced(L):
     st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
     assert st == lowm.LOWM_OK
     assert (t["tile_n"], t["m_pad"], t["split_k"], t["block_k"]) == (64, 8, 2, 64)
-    assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["pdl"] == 1
-    assert t["stages"] >= 10 and t["smem_bytes"] <= 232448
+    assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["pdl"] == 1 and t["persistent"] == 0
+    assert t["stages"] * t["kb_per_stage"] >= 8 and t["smem_bytes"] <= 232448
+    assert t["kb_per_stage"] == 4          # 32 blocks per rank: 4 per 3-D copy
 
 
-@pytest.mark.parametrize("M,N,K,sk,ctas", [(4, 2304, 12288, 4, 144), (4, 49152, 4096, 2, 1536),
-                                          (16, 6144, 32768, 4, 384), (64, 6144, 4096, 1, 96)])
-def test_cluster_counts_for_the_workloads(L, M, N, K, sk, ctas):
+@pytest.mark.parametrize("M,N,K,sk", [(4, 2304, 12288, 4), (4, 49152, 4096, 2), (16, 6144, 32768, 4),
+                                      (64, 6144, 4096, 1), (4, 6144, 4096, 2)])
+def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
-    assert st == lowm.LOWM_OK and t["ctas"] == ctas and t["split_k"] == sk
+    assert st == lowm.LOWM_OK and t["split_k"] == sk and t["tiles"] == N // 64
     assert t["m_pad"] == (8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64)
+    assert t["ctas"] == t["num_clusters"] * sk
+    if t["persistent"]:
+        # every cluster gets ceil(tiles / clusters) tiles and none is idle
+        per = t["tiles_per_cluster"]
+        assert per >= 2 and (per - 1) * t["num_clusters"] < t["tiles"] <= per * t["num_clusters"]
+    else:
+        assert t["num_clusters"] == t["tiles"] and t["tiles_per_cluster"] == 1
+
+
+@pytest.mark.parametrize("M,K,sk,want", [(4, 64 * 3, 1, 1), (4, 64 * 6, 1, 2), (4, 64 * 8, 2, 4), (4, 64 * 5, 1, 1),
+                                        (64, 1024, 8, 2), (64, 4096, 8, 2), (16, 32768, 4, 4)])
+def test_kb_per_stage_divides_the_rank_and_fits(L, M, K, sk, want):
+    st, t = lowm.lowm_gemm_query_tactic(M, 256, K, sk)
+    assert st == lowm.LOWM_OK
+    kbr = K // (sk * 64)
+    assert kbr % t["kb_per_stage"] == 0 and t["kb_per_stage"] == want
+    assert t["smem_bytes"] <= 232448 and t["stages"] >= 2
+
+
+def test_kb_per_stage_override(L, monkeypatch):
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", "8")
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and t["kb_per_stage"] == 8
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", "8")
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 64 * 6, 1)      # 6 blocks: 8 does not divide, default 2
+    assert st == lowm.LOWM_OK and t["kb_per_stage"] == 2
+
+
+def test_persistent_override_and_cap(L, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", "4")
+    st, t = lowm.lowm_gemm_query_tactic(4, 13 * 64, 1024, 2)
+    assert st == lowm.LOWM_OK and t["persistent"] == 1
+    assert t["num_clusters"] == 4 and t["tiles_per_cluster"] == 4 and t["ctas"] == 8
+    monkeypatch.setenv("LOWM_PERSISTENT", "0")
+    st, t = lowm.lowm_gemm_query_tactic(4, 49152, 4096, 2)
+    assert st == lowm.LOWM_OK and t["persistent"] == 0 and t["ctas"] == 1536
 
 
 def test_auto_split_k_keeps_the_k_loop_non_empty(L):
@@ -94,6 +132,7 @@ def test_gemm_rejects_null_and_misaligned_pointers_before_touching_a_device(L):
         == lowm.LOWM_ERR_INVALID_ARGUMENT
     assert lowm.lowm_gemm_bf16_host(0, 1, 1, 1, 1, 1, 4, 64, 64, 0, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
     assert lowm.lowm_tmem_hog_launch(0, 1, 48, 1) == lowm.LOWM_ERR_INVALID_ARGUMENT
+    assert lowm.lowm_gemm_bf16_ex(0x1000, 0x100000, 0x200000, 4, 64, 64, 1, 2, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
 
 
 def test_library_does_not_reference_the_oracle():

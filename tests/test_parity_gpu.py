@@ -206,9 +206,12 @@ def test_host_buffer_entry_point_matches_device_path():
     assert np.array_equal(inputs.bits(Ch), C_dev)
 
 
-def test_full_capacity_request_gives_the_same_bits():
+def test_shipped_tactic_with_full_capacity_request_gives_the_same_bits(monkeypatch):
+    # The pages' shipped tactic: 10 stages of one 64-wide K block, full-capacity
+    # shared-memory request (nothing else can co-reside on the SM).
     A, W = inputs.make_problem(4, 6144, 4096, seed=8)
     C1, _ = run_gpu(A, W, 2, want_f32=False)
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", "1")
     C2, _ = run_gpu(A, W, 2, want_f32=False, full_smem=1, stages=10)
     assert np.array_equal(C1, C2)
 
@@ -225,4 +228,108 @@ def test_a_dropped_mailbox_times_out_and_the_context_survives():
     st, detail = lowm.lowm_gemm_sync_status()
     assert st == lowm.LOWM_ERR_TIMEOUT and detail == (1 << 8), (st, hex(detail))
     # the status word was cleared and the context still works
+    check(A, W, 2)
+
+
+def test_w_before_pdl_wait_flag_keeps_the_chain_correct():
+    # W is never written by the preceding kernel here, so the flag's promise holds;
+    # A is the previous GEMM's output and must still be read after the wait.
+    M, D = 4, 2048
+    A0, _ = inputs.make_problem(M, D, D, seed=12)
+    Ws = [inputs.make_problem(M, D, D, seed=40 + i)[1] for i in range(6)]
+    Wd = [w.to(DEV) for w in Ws]
+    Cs = [A0.to(DEV)] + [torch.empty((M, D), dtype=torch.bfloat16, device=DEV) for _ in Ws]
+    for i, w in enumerate(Wd):
+        st = lowm.lowm_gemm_bf16_ex(Cs[i], w, Cs[i + 1], M, D, D, 2, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT, None)
+        assert st == lowm.LOWM_OK
+    sync_ok()
+    for i, w in enumerate(Wd):
+        ref = torch.empty((M, D), dtype=torch.bfloat16, device=DEV)
+        assert lowm.lowm_gemm_bf16(Cs[i], w, ref, M, D, D, 2, None) == lowm.LOWM_OK
+        sync_ok()
+        assert torch.equal(ref.view(torch.int16), Cs[i + 1].view(torch.int16)), "link %d" % i
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (4, 49152, 4096, 2), (64, 192, 1024, 8),
+                                           (3, 64, 64, 1)])
+def test_w_before_pdl_wait_flag_gives_the_same_bits(M, N, K, split_k):
+    A, W = inputs.make_problem(M, N, K, seed=13)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    c0 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    c1 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16(Ad, Wd, c0, M, N, K, split_k, None) == lowm.LOWM_OK
+    assert lowm.lowm_gemm_bf16_ex(Ad, Wd, c1, M, N, K, split_k, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT, None) \
+        == lowm.LOWM_OK
+    sync_ok()
+    assert torch.equal(c0.view(torch.int16), c1.view(torch.int16))
+
+
+# ---------------------------------------------------------------- persistent schedule
+PERSISTENT = [
+    # M, N, K, split_k, max clusters: several tiles per cluster, uneven tile counts, ring wrap across tiles
+    (4, 13 * 64, 1024, 2, 4), (1, 7 * 64, 512, 1, 3), (8, 9 * 64, 2048, 4, 2), (5, 10 * 64, 1024, 8, 3),
+    (16, 6 * 64, 4096, 2, 2), (32, 5 * 64, 1024, 1, 2), (64, 6 * 64, 2048, 2, 3), (3, 2 * 64, 256, 2, 1),
+]
+
+
+@pytest.mark.parametrize("M,N,K,split_k,cap", PERSISTENT)
+def test_persistent_schedule_random(M, N, K, split_k, cap, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", str(cap))
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK and t["persistent"] == 1 and t["num_clusters"] <= cap
+    A, W = inputs.make_problem(M, N, K, seed=300 + M + N + K)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("M,N,K,split_k,cap", [(16, 12 * 64, 4096, 4, 5), (4, 11 * 64, 2048, 2, 3)])
+def test_persistent_schedule_integer_exact(M, N, K, split_k, cap, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", str(cap))
+    A, W = inputs.make_problem(M, N, K, seed=8, kind="int")
+    check(A, W, split_k, exact=True)
+
+
+def test_persistent_and_one_tile_schedules_agree_bitwise(monkeypatch):
+    M, N, K, sk = 4, 6144, 4096, 2
+    A, W = inputs.make_problem(M, N, K, seed=21)
+    monkeypatch.setenv("LOWM_PERSISTENT", "0")
+    C0, _ = run_gpu(A, W, sk, want_f32=False)
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", "40")
+    C1, _ = run_gpu(A, W, sk, want_f32=False)
+    assert np.array_equal(C0, C1)
+
+
+# ---------------------------------------------------------------- K blocks per stage
+@pytest.mark.parametrize("kbs", [1, 2, 4, 8])
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 640, 2048, 2), (8, 192, 4096, 1), (3, 128, 4096, 8)])
+def test_every_kb_per_stage_random(kbs, M, N, K, split_k, monkeypatch):
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", str(kbs))
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK and t["kb_per_stage"] == kbs
+    A, W = inputs.make_problem(M, N, K, seed=500 + kbs + M)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 256, 64 * 3, 1), (5, 128, 64 * 5, 1), (16, 192, 64 * 6, 1),
+                                           (64, 128, 64 * 12, 2), (33, 64, 64 * 14, 2)])
+def test_block_counts_not_divisible_by_four(M, N, K, split_k):
+    A, W = inputs.make_problem(M, N, K, seed=600 + K)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("kbs", [1, 4])
+def test_kb_per_stage_integer_exact(kbs, monkeypatch):
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", str(kbs))
+    A, W = inputs.make_problem(16, 256, 4096, seed=9, kind="int")
+    check(A, W, 2, exact=True)
+
+
+@pytest.mark.parametrize("kbs", [1, 4])
+def test_persistent_with_kb_per_stage(kbs, monkeypatch):
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", str(kbs))
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", "5")
+    A, W = inputs.make_problem(4, 17 * 64, 2048, seed=10)
     check(A, W, 2)
