@@ -312,6 +312,18 @@ def run_ours(args):
             "gbs": wbytes * wide_steps / wsecs / 1e9, "steps": wide_steps,
             "frac": wbytes * wide_steps / wsecs / 1e9 / peak, "l2": "rotating %d W copies" % wR}
 
+    # The same workload through lowm_gemm_bf16_ex with LOWM_FLAG_W_BEFORE_PDL_WAIT
+    # (W copies are never written by a kernel, so the flag's promise holds).
+    variants = {}
+    if not w["flags"]:
+        vw = dict(w, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
+        vsteps = min(args.steps, 50000)
+        vsecs, _, _ = time_device(lowm, vw, vsteps, max(args.warmup, 3), device)
+        variants["w_before_pdl_wait"] = {"us_per_gemm": vsecs / vsteps * 1e6,
+                                         "gbs": bytes_per * vsteps / vsecs / 1e9,
+                                         "frac": bytes_per * vsteps / vsecs / 1e9 / peak, "steps": vsteps,
+                                         "entry_point": "lowm_gemm_bf16_ex(flags=LOWM_FLAG_W_BEFORE_PDL_WAIT)"}
+
     e2e_steps = max(5, min(args.steps, 50))
     esecs, h2d, d2h = time_e2e(lowm, w, e2e_steps, device)
     e2e = {"value": bytes_per * e2e_steps / esecs / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -338,6 +350,7 @@ def run_ours(args):
                      else "fallback 6800 GB/s", "kernel": KERNEL_NAME,
                      "algorithmic_bytes_per_launch": bytes_per, "traffic": committed_traffic(w)},
         "wide_n": wide,
+        "variants": variants,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,

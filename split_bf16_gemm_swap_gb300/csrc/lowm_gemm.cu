@@ -99,28 +99,56 @@ int footprint(int m_pad, int split_k, int stages, int kbs, int bufs)
     return (int)lowm::make_smem_layout(m_pad, split_k, stages, kbs, bufs).bytes;
 }
 
-// Deepest ring (at least 2 stages) that lets `ctas_per_sm` CTAs share one SM.
-int stages_for(int m_pad, int split_k, int kbs, int ctas_per_sm, int bufs)
-{
-    const int budget = kSmemPerSm / ctas_per_sm - kSmemReservedPerCta;
-    int s = 2;
-    while (s < 32 && footprint(m_pad, split_k, s + 1, kbs, bufs) <= budget &&
-           footprint(m_pad, split_k, s + 1, kbs, bufs) <= kMaxSmemPerCta)
-        ++s;
-    return s;
-}
+// Ring shape (K blocks per stage x stages) for a launch of `ctas` CTAs on
+// `sms` SMs.  From measurements on GB300 (M4 N6144/2304/49152, M16 K32768):
+//   - every copy costs a fixed per-CTA time, so blocks per copy matter most;
+//   - a grid that does not fit on the GPU at once wants several small CTAs per
+//     SM (their prologues and epilogues overlap each other's streams): three
+//     per SM without clusters, five with them;
+//   - rings beyond ~160 KiB per CTA gain nothing.
+// Hence: budget shared memory for ceil(ctas / sms) CTAs per SM when that is at
+// most 4 (the whole grid resident at once), else for 3 (split_k 1) or 5; take
+// the most blocks per copy (8, 4, 2, 1, dividing the rank's blocks) whose
+// 2-stage ring fits, then the most stages that fit.  LOWM_KB_PER_STAGE and
+// LOWM_STAGES override (tuning).
+struct Ring {
+    int kbs, stages;
+};
 
-// K blocks per stage: the largest of 4, 2, 1 that divides the rank's block
-// count (LOWM_KB_PER_STAGE=1/2/4/8 overrides when it divides, for tuning).
-int choose_kb_per_stage(int kb_per_rank)
+constexpr int kMaxRingBytes = 160 * 1024;
+
+Ring choose_ring(int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int bufs)
 {
-    const int force = env_int("LOWM_KB_PER_STAGE", 0);
-    if ((force == 1 || force == 2 || force == 4 || force == 8) && kb_per_rank % force == 0)
-        return force;
-    for (int b = 4; b > 1; b /= 2)
-        if (kb_per_rank % b == 0)
-            return b;
-    return 1;
+    const int per_sm_one_wave = (ctas + std::max(1, sms) - 1) / std::max(1, sms);
+    const int per_sm = per_sm_one_wave <= 4 ? std::max(1, per_sm_one_wave) : (split_k == 1 ? 3 : 5);
+    const int budget = std::min(kMaxSmemPerCta, kSmemPerSm / per_sm - kSmemReservedPerCta);
+    int force_kbs = env_int("LOWM_KB_PER_STAGE", 0);
+    if (force_kbs != 1 && force_kbs != 2 && force_kbs != 4 && force_kbs != 8)
+        force_kbs = 0;
+    if (force_kbs && kb_per_rank % force_kbs != 0)
+        force_kbs = 0;                                 // a forced value that does not divide is ignored
+    const int force_st = env_int("LOWM_STAGES", 0);
+    auto ring_bytes = [&](int kbs, int st) { return st * kbs * (int)(lowm::kWBlockBytes + (uint32_t)m_pad * 128u); };
+    int kbs = 1;
+    if (force_kbs) {
+        kbs = force_kbs;
+    } else {
+        for (int b = 8; b >= 1; b /= 2)
+            if (kb_per_rank % b == 0 && footprint(m_pad, split_k, 2, b, bufs) <= budget &&
+                ring_bytes(b, 2) <= kMaxRingBytes) {
+                kbs = b;
+                break;
+            }
+    }
+    int st = 2;
+    if (force_st >= 2) {
+        st = force_st;
+    } else {
+        while (st < 32 && footprint(m_pad, split_k, st + 1, kbs, bufs) <= budget &&
+               ring_bytes(kbs, st + 1) <= kMaxRingBytes)
+            ++st;
+    }
+    return Ring{kbs, st};
 }
 
 bool shape_ok(int M, int N, int K, int split_k)
@@ -255,37 +283,31 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     const int m_pad = m_pad_of(M);
     const int tiles = N / lowm::kTileN;
-    int kbs = choose_kb_per_stage(K / (split_k * lowm::kBlockK));
-    while (kbs > 1 && footprint(m_pad, split_k, 2, kbs, 1) > kMaxSmemPerCta)
-        kbs /= 2;                                       // a 2-stage ring must fit
-    if (stages_override <= 0)
-        stages_override = env_int("LOWM_STAGES", 0);   // tuning hook: replaces the default ring depth
+    const int kbr = K / (split_k * lowm::kBlockK);
     if (stages_override == 1)
         return LOWM_ERR_INVALID_ARGUMENT;
-    // Two CTAs per SM by default: one CTA's prologue and epilogue overlap the
-    // other's stream, and the next kernel's CTAs (PDL) can start early.
-    auto plan = [&](int bufs, int &stages, int &fp) {
-        stages = stages_override >= 2 ? stages_override : stages_for(m_pad, split_k, kbs, 2, bufs);
-        fp = footprint(m_pad, split_k, stages, kbs, bufs);
-    };
-    int stages = 0, fp = 0;
-    plan(1, stages, fp);
+    const int nsm = sms > 0 ? sms : 152;
+    // The persistent schedule is opt-in (LOWM_PERSISTENT=1).
+    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1;
+    int clusters = tiles;
+    Ring ring = choose_ring(m_pad, split_k, kbr, tiles * split_k, nsm, 1);
+    if (stages_override >= 2)
+        ring.stages = stages_override;
+    int fp = footprint(m_pad, split_k, ring.stages, ring.kbs, 1);
     if (fp > kMaxSmemPerCta)
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     int smem = full_smem ? kMaxSmemPerCta : fp;
-    // The persistent schedule is opt-in (LOWM_PERSISTENT=1) until it measures
-    // faster than one tile per cluster on the shapes it targets.
-    const bool persistent_wanted = env_int("LOWM_PERSISTENT", 0) == 1;
-    bool persistent = persistent_wanted;
-    int clusters = tiles;
     if (persistent) {
-        int st2 = 0, fp2 = 0;
-        plan(2, st2, fp2);
+        // Size the persistent grid for the CTAs that fit at the chosen footprint.
+        Ring pr = choose_ring(m_pad, split_k, kbr, tiles * split_k, nsm, 2);
+        if (stages_override >= 2)
+            pr.stages = stages_override;
+        const int fp2 = footprint(m_pad, split_k, pr.stages, pr.kbs, 2);
         if (fp2 <= kMaxSmemPerCta) {
-            stages = st2;
+            ring = pr;
             fp = fp2;
             smem = full_smem ? kMaxSmemPerCta : fp;
-            int fit = std::max(1, resident_clusters(m_pad, split_k, smem, sms, true, have_device));
+            int fit = std::max(1, resident_clusters(m_pad, split_k, smem, nsm, true, have_device));
             const int cap = env_int("LOWM_MAX_CLUSTERS", 0);   // tuning / test hook: fewer clusters
             if (cap > 0)
                 fit = std::min(fit, cap);
@@ -295,6 +317,8 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
             persistent = false;
         }
     }
+    const int stages = ring.stages;
+    const int kbs = ring.kbs;
     t->tile_n = lowm::kTileN;
     t->m_pad = m_pad;
     t->split_k = split_k;
