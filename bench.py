@@ -73,17 +73,20 @@ def measured_peak():
 
 
 def kernel_sources_sha():
+    """Fingerprint of the device code (the kernels and their PTX wrappers)."""
     h = hashlib.sha256()
-    for rel in ("split_bf16_gemm_swap_gb300/csrc/lowm_kernel.cuh", "split_bf16_gemm_swap_gb300/csrc/ptx.cuh",
-                "split_bf16_gemm_swap_gb300/csrc/lowm_gemm.cu"):
+    for rel in ("split_bf16_gemm_swap_gb300/csrc/lowm_kernel.cuh", "split_bf16_gemm_swap_gb300/csrc/lowm_persistent.cuh",
+                "split_bf16_gemm_swap_gb300/csrc/ptx.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
-    path = os.path.join(ROOT, "profiles", "lowm_splitk_kernel_traffic.md")
+def committed_traffic(workload, tactic):
+    """DRAM bytes per launch from the committed ncu summary of this workload, if it
+    was taken on the current device code with the same ring."""
+    path = os.path.join(ROOT, "profiles", "lowm_splitk_kernel_m%d_n%d_k%d.md" % (
+        workload["M"], workload["N"], workload["K"]))
     try:
         fields = {}
         for line in open(path):
@@ -93,6 +96,8 @@ def committed_traffic(workload):
         if fields.get("kernel_sources_sha256_16") != kernel_sources_sha():
             return None
         if fields.get("workload") != workload_name(workload):
+            return None
+        if fields.get("ring") != "%d x %d" % (tactic["kb_per_stage"], tactic["stages"]):
             return None
         return int(fields["dram_bytes_per_launch"])
     except Exception:
@@ -283,7 +288,10 @@ def run_ours(args):
         torch.distributed.barrier()
     from split_bf16_gemm_swap_gb300 import lowm
     lowm.lib()
-    w = dict(WORKLOAD, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT if args.w_before_pdl_wait else 0)
+    # The W copies are never written by any kernel, so the promise of
+    # LOWM_FLAG_W_BEFORE_PDL_WAIT holds; --default-launch measures the plain
+    # lowm_gemm_bf16 path instead (also reported under "variants").
+    w = dict(WORKLOAD, flags=0 if args.default_launch else lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     st, tactic = lowm.lowm_gemm_query_tactic(w["M"], w["N"], w["K"], w["split_k"])
     assert st == 0, lowm.status_string(st)
     peak, peak_kind = measured_peak()
@@ -308,21 +316,22 @@ def run_ours(args):
     wide_w = dict(WIDE, flags=w["flags"])
     wsecs, _, wR = time_device(lowm, wide_w, wide_steps, max(args.warmup, 3), device)
     wbytes = algo_bytes(WIDE["M"], WIDE["N"], WIDE["K"])
-    wide = {"workload": workload_name(WIDE), "us_per_gemm": wsecs / wide_steps * 1e6,
+    _, wtactic = lowm.lowm_gemm_query_tactic(WIDE["M"], WIDE["N"], WIDE["K"], WIDE["split_k"])
+    wide = {"workload": workload_name(WIDE), "us_per_gemm": wsecs / wide_steps * 1e6, "tactic": wtactic,
+            "traffic": committed_traffic(WIDE, wtactic),
             "gbs": wbytes * wide_steps / wsecs / 1e9, "steps": wide_steps,
             "frac": wbytes * wide_steps / wsecs / 1e9 / peak, "l2": "rotating %d W copies" % wR}
 
-    # The same workload through lowm_gemm_bf16_ex with LOWM_FLAG_W_BEFORE_PDL_WAIT
-    # (W copies are never written by a kernel, so the flag's promise holds).
+    # The same workload through the other launch path (default flags <-> the
+    # W-before-PDL-wait flag), same protocol.
     variants = {}
-    if not w["flags"]:
-        vw = dict(w, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
-        vsteps = min(args.steps, 50000)
-        vsecs, _, _ = time_device(lowm, vw, vsteps, max(args.warmup, 3), device)
-        variants["w_before_pdl_wait"] = {"us_per_gemm": vsecs / vsteps * 1e6,
-                                         "gbs": bytes_per * vsteps / vsecs / 1e9,
-                                         "frac": bytes_per * vsteps / vsecs / 1e9 / peak, "steps": vsteps,
-                                         "entry_point": "lowm_gemm_bf16_ex(flags=LOWM_FLAG_W_BEFORE_PDL_WAIT)"}
+    vw = dict(w, flags=0 if w["flags"] else lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    vsteps = min(args.steps, 50000)
+    vsecs, _, _ = time_device(lowm, vw, vsteps, max(args.warmup, 3), device)
+    variants["default_flags" if vw["flags"] == 0 else "w_before_pdl_wait"] = {
+        "us_per_gemm": vsecs / vsteps * 1e6, "gbs": bytes_per * vsteps / vsecs / 1e9,
+        "frac": bytes_per * vsteps / vsecs / 1e9 / peak, "steps": vsteps,
+        "entry_point": "lowm_gemm_bf16_ex(flags=%d)" % vw["flags"]}
 
     e2e_steps = max(5, min(args.steps, 50))
     esecs, h2d, d2h = time_e2e(lowm, w, e2e_steps, device)
@@ -344,11 +353,12 @@ def run_ours(args):
                    "tactic": tactic, "launch": "CUDA graphs of 100 PDL launches, replayed",
                    "entry_point": "lowm_gemm_bf16_ex(flags=%d)" % w["flags"],
                    "w_before_pdl_wait": bool(w["flags"]),
+                   "w_before_pdl_wait_note": "W is never written by a kernel here, so the flag's promise holds",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
                      else "fallback 6800 GB/s", "kernel": KERNEL_NAME,
-                     "algorithmic_bytes_per_launch": bytes_per, "traffic": committed_traffic(w)},
+                     "algorithmic_bytes_per_launch": bytes_per, "traffic": committed_traffic(w, tactic)},
         "wide_n": wide,
         "variants": variants,
         "e2e": e2e,
@@ -462,8 +472,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--w-before-pdl-wait", action="store_true",
-                    help="launch with LOWM_FLAG_W_BEFORE_PDL_WAIT (the W copies are never written by a kernel)")
+    ap.add_argument("--default-launch", action="store_true",
+                    help="time lowm_gemm_bf16 without LOWM_FLAG_W_BEFORE_PDL_WAIT (the headline uses the flag: "
+                         "the W copies are never written by a kernel)")
     ap.add_argument("--profile-only", action="store_true",
                     help="plain launches of the workload for a profiler (no timing, no JSON line)")
     ap.add_argument("--wide", action="store_true", help="with --profile-only: the wide-N workload")

@@ -18,11 +18,46 @@
 #include <unordered_map>
 
 #include "../../include/lowm_gemm.h"
-#include "lowm_kernel.cuh"
-#include "lowm_persistent.cuh"
+#include "lowm_kernels.h"
+
+namespace lowm {
+
+// The device status word: kernels set bits of the waits that gave up (through
+// the pointer in their parameters); lowm_gemm_sync_status reads and clears it.
+__device__ unsigned int g_lowm_status;
+
+// The concurrent TMEM allocator of the stress method: allocate, fill with NaN,
+// free.  128 threads; never waits on another kernel.
+__global__ void __launch_bounds__(128) tmem_hog_kernel(int ncols, int iters)
+{
+    __shared__ uint32_t slot;
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        ptx::tmem_alloc(ptx::smem_u32(&slot), (uint32_t)ncols);
+        ptx::tmem_relinquish_alloc_permit();
+    }
+    ptx::tcgen05_fence_before_thread_sync();
+    __syncthreads();
+    ptx::tcgen05_fence_after_thread_sync();
+    const uint32_t base = slot + ((uint32_t)(32 * warp) << 16);
+    const uint32_t nan8[8] = {0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u,
+                              0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u};
+    for (int it = 0; it < iters; ++it)
+        for (int c = 0; c < ncols; c += 8)
+            ptx::tmem_st_32x32b_x8(base + (uint32_t)c, nan8);
+    ptx::tmem_wait_st();
+    ptx::tcgen05_fence_before_thread_sync();
+    __syncthreads();
+    ptx::tcgen05_fence_after_thread_sync();
+    if (warp == 0)
+        ptx::tmem_dealloc(slot, (uint32_t)ncols);
+}
+
+}  // namespace lowm
 
 namespace {
 
+using lowm::KernelFn;
 using lowm::KernelParams;
 using lowm::SmemLayout;
 
@@ -94,9 +129,9 @@ int m_pad_of(int M)
     return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
 }
 
-int footprint(int m_pad, int split_k, int stages, int kbs, int bufs)
+int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs)
 {
-    return (int)lowm::make_smem_layout(m_pad, split_k, stages, kbs, bufs).bytes;
+    return (int)lowm::make_smem_layout(tile_n, m_pad, split_k, stages, kbs, bufs).bytes;
 }
 
 // Ring shape (K blocks per stage x stages) for a launch of `ctas` CTAs on
@@ -117,7 +152,7 @@ struct Ring {
 
 constexpr int kMaxRingBytes = 160 * 1024;
 
-Ring choose_ring(int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int bufs)
+Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int bufs)
 {
     const int per_sm_one_wave = (ctas + std::max(1, sms) - 1) / std::max(1, sms);
     const int per_sm = per_sm_one_wave <= 4 ? std::max(1, per_sm_one_wave) : (split_k == 1 ? 3 : 5);
@@ -128,13 +163,13 @@ Ring choose_ring(int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int
     if (force_kbs && kb_per_rank % force_kbs != 0)
         force_kbs = 0;                                 // a forced value that does not divide is ignored
     const int force_st = env_int("LOWM_STAGES", 0);
-    auto ring_bytes = [&](int kbs, int st) { return st * kbs * (int)(lowm::kWBlockBytes + (uint32_t)m_pad * 128u); };
+    auto ring_bytes = [&](int kbs, int st) { return st * kbs * (int)(lowm::w_block_bytes(tile_n) + (uint32_t)m_pad * 128u); };
     int kbs = 1;
     if (force_kbs) {
         kbs = force_kbs;
     } else {
         for (int b = 8; b >= 1; b /= 2)
-            if (kb_per_rank % b == 0 && footprint(m_pad, split_k, 2, b, bufs) <= budget &&
+            if (kb_per_rank % b == 0 && footprint(tile_n, m_pad, split_k, 2, b, bufs) <= budget &&
                 ring_bytes(b, 2) <= kMaxRingBytes) {
                 kbs = b;
                 break;
@@ -144,7 +179,7 @@ Ring choose_ring(int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int
     if (force_st >= 2) {
         st = force_st;
     } else {
-        while (st < 32 && footprint(m_pad, split_k, st + 1, kbs, bufs) <= budget &&
+        while (st < 32 && footprint(tile_n, m_pad, split_k, st + 1, kbs, bufs) <= budget &&
                ring_bytes(kbs, st + 1) <= kMaxRingBytes)
             ++st;
     }
@@ -153,15 +188,16 @@ Ring choose_ring(int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int
 
 bool shape_ok(int M, int N, int K, int split_k)
 {
-    return M >= 1 && M <= 64 && N > 0 && N % lowm::kTileN == 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
+    return M >= 1 && M <= 64 && N > 0 && N % 64 == 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
 }
 
 // split_k = 0: the smallest split (1, 2, 4, 8) that keeps the K loop non-empty
-// and gives at least one CTA per SM, preferring fewer cluster reductions.
+// and gives at least one CTA per SM (counted in 64-column tiles), preferring
+// fewer cluster reductions.
 int choose_split_k(int M, int N, int K, int sms)
 {
     (void)M;
-    const int tiles = N / lowm::kTileN;
+    const int tiles = N / 64;
     int best = 0;
     for (int sk = 1; sk <= 8; sk *= 2) {
         if (K % (sk * lowm::kBlockK) != 0)
@@ -174,36 +210,31 @@ int choose_split_k(int M, int N, int K, int sms)
 }
 
 // ------------------------------------------------------------------ kernels
-typedef void (*KernelFn)(CUtensorMap, CUtensorMap, KernelParams);
-
-template <int MP, int SK>
-KernelFn kernel_ptr(bool persistent)
+KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent)
 {
-    return persistent ? reinterpret_cast<KernelFn>(&lowm::lowm_splitk_persistent_kernel<MP, SK>)
-                      : reinterpret_cast<KernelFn>(&lowm::lowm_splitk_kernel<MP, SK>);
+    if (tile_n == 64)
+        return lowm::kernel_tile64(m_pad, sk, persistent);
+    if (tile_n == 128)
+        return lowm::kernel_tile128(m_pad, sk, persistent);
+    return nullptr;
 }
 
-template <int MP>
-KernelFn kernel_for_split(int sk, bool persistent)
+// Device address of the status word on the current device (looked up once per device).
+unsigned int *status_word()
 {
-    switch (sk) {
-    case 1: return kernel_ptr<MP, 1>(persistent);
-    case 2: return kernel_ptr<MP, 2>(persistent);
-    case 4: return kernel_ptr<MP, 4>(persistent);
-    case 8: return kernel_ptr<MP, 8>(persistent);
-    default: return nullptr;
+    static std::mutex mu;
+    static unsigned int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, lowm::g_lowm_status) != cudaSuccess)
+            return nullptr;
+        addr[dev] = static_cast<unsigned int *>(p);
     }
-}
-
-KernelFn kernel_for(int m_pad, int sk, bool persistent)
-{
-    switch (m_pad) {
-    case 8: return kernel_for_split<8>(sk, persistent);
-    case 16: return kernel_for_split<16>(sk, persistent);
-    case 32: return kernel_for_split<32>(sk, persistent);
-    case 64: return kernel_for_split<64>(sk, persistent);
-    default: return nullptr;
-    }
+    return addr[dev];
 }
 
 lowm_status_t prepare_kernel(KernelFn fn)
@@ -228,13 +259,13 @@ lowm_status_t prepare_kernel(KernelFn fn)
 // Clusters of `split_k` CTAs that fit on the GPU at once with `smem` bytes
 // each: the occupancy API when a usable device is current, else the per-SM
 // arithmetic (shared memory and threads).
-int resident_clusters(int m_pad, int split_k, int smem, int sms, bool persistent, bool have_device)
+int resident_clusters(int tile_n, int m_pad, int split_k, int smem, int sms, bool persistent, bool have_device)
 {
     const int per_sm = std::min(kSmemPerSm / (smem + kSmemReservedPerCta), 2048 / lowm::kThreads);
     const int formula = sms * per_sm / split_k;
     if (!have_device)
         return formula;
-    KernelFn fn = kernel_for(m_pad, split_k, persistent);
+    KernelFn fn = kernel_for(tile_n, m_pad, split_k, persistent);
     if (!fn || prepare_kernel(fn) != LOWM_OK)
         return formula;
     static std::mutex mu;
@@ -281,33 +312,60 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         split_k = choose_split_k(M, N, K, sms > 0 ? sms : 152);
     if (split_k == 0 || !shape_ok(M, N, K, split_k))
         return LOWM_ERR_UNSUPPORTED_SHAPE;
-    const int m_pad = m_pad_of(M);
-    const int tiles = N / lowm::kTileN;
     const int kbr = K / (split_k * lowm::kBlockK);
     if (stages_override == 1)
         return LOWM_ERR_INVALID_ARGUMENT;
     const int nsm = sms > 0 ? sms : 152;
+    // Tile width.  128-column tiles (MMA M = 128: every epilogue lane holds a
+    // row, and each W copy is twice as large) measured faster for m_pad >= 32
+    // (M4..64 sweep at N6144 K4096); for m_pad 8 and 16, 64-column tiles
+    // were as fast or faster.  LOWM_TILE_N = 64 / 128 overrides when the shape
+    // allows it (tuning).
+    int tile_n = 64;
+    {
+        const int force = env_int("LOWM_TILE_N", 0);
+        const bool can128 = N % 128 == 0;
+        if (force == 128 && can128)
+            tile_n = 128;
+        else if (force != 64 && can128 && m_pad_of(M) >= 32)
+            tile_n = 128;
+    }
+    int m_pad = m_pad_of(M);
+    if (tile_n == 128 && m_pad < 16)
+        m_pad = 16;                                     // MMA M = 128 needs N a multiple of 16
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1).
     bool persistent = env_int("LOWM_PERSISTENT", 0) == 1;
+    int tiles = N / tile_n;
     int clusters = tiles;
-    Ring ring = choose_ring(m_pad, split_k, kbr, tiles * split_k, nsm, 1);
+    Ring ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
     if (stages_override >= 2)
         ring.stages = stages_override;
-    int fp = footprint(m_pad, split_k, ring.stages, ring.kbs, 1);
+    int fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1);
+    if (fp > kMaxSmemPerCta && tile_n == 128) {
+        // e.g. m_pad 64 with split_k 8: the 128-column mailbox does not fit; use 64 columns
+        tile_n = 64;
+        m_pad = m_pad_of(M);
+        tiles = N / tile_n;
+        clusters = tiles;
+        ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
+        if (stages_override >= 2)
+            ring.stages = stages_override;
+        fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1);
+    }
     if (fp > kMaxSmemPerCta)
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     int smem = full_smem ? kMaxSmemPerCta : fp;
     if (persistent) {
         // Size the persistent grid for the CTAs that fit at the chosen footprint.
-        Ring pr = choose_ring(m_pad, split_k, kbr, tiles * split_k, nsm, 2);
+        Ring pr = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 2);
         if (stages_override >= 2)
             pr.stages = stages_override;
-        const int fp2 = footprint(m_pad, split_k, pr.stages, pr.kbs, 2);
+        const int fp2 = footprint(tile_n, m_pad, split_k, pr.stages, pr.kbs, 2);
         if (fp2 <= kMaxSmemPerCta) {
             ring = pr;
             fp = fp2;
             smem = full_smem ? kMaxSmemPerCta : fp;
-            int fit = std::max(1, resident_clusters(m_pad, split_k, smem, nsm, true, have_device));
+            int fit = std::max(1, resident_clusters(tile_n, m_pad, split_k, smem, nsm, true, have_device));
             const int cap = env_int("LOWM_MAX_CLUSTERS", 0);   // tuning / test hook: fewer clusters
             if (cap > 0)
                 fit = std::min(fit, cap);
@@ -319,7 +377,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     }
     const int stages = ring.stages;
     const int kbs = ring.kbs;
-    t->tile_n = lowm::kTileN;
+    t->tile_n = tile_n;
     t->m_pad = m_pad;
     t->split_k = split_k;
     t->stages = stages;
@@ -429,7 +487,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     st = make_tactic(M, N, K, split_k, sms, true, dbg ? dbg->stages : 0, (dbg && dbg->full_smem) ? 1 : 0, &t);
     if (st != LOWM_OK)
         return st;
-    KernelFn fn = kernel_for(t.m_pad, t.split_k, t.persistent != 0);
+    KernelFn fn = kernel_for(t.tile_n, t.m_pad, t.split_k, t.persistent != 0);
     if (!fn)
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     if ((st = prepare_kernel(fn)) != LOWM_OK)
@@ -437,12 +495,15 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     CUtensorMap map_a, map_w;
     if ((st = get_map(A, M, K, t.m_pad, t.kb_per_stage, &map_a)) != LOWM_OK)
         return st;
-    if ((st = get_map(W, N, K, lowm::kTileN, t.kb_per_stage, &map_w)) != LOWM_OK)
+    if ((st = get_map(W, N, K, t.tile_n, t.kb_per_stage, &map_w)) != LOWM_OK)
         return st;
 
     KernelParams p;
     std::memset(&p, 0, sizeof p);
     p.C = reinterpret_cast<__nv_bfloat16 *>(C);
+    p.status = status_word();
+    if (!p.status)
+        return LOWM_ERR_CUDA;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -471,7 +532,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     cfg.blockDim = dim3(lowm::kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)t.smem_bytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attrs[2];
+    cudaLaunchAttribute attrs[3];
     int na = 0;
     if (t.split_k > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
@@ -479,6 +540,14 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
         attrs[na].val.clusterDim.y = 1;
         attrs[na].val.clusterDim.z = 1;
         ++na;
+        // Tuning hook: LOWM_CLUSTER_POLICY = 1 (spread) or 2 (load balancing).
+        const int pol = env_int("LOWM_CLUSTER_POLICY", 0);
+        if (pol == 1 || pol == 2) {
+            attrs[na].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+            attrs[na].val.clusterSchedulingPolicyPreference =
+                pol == 1 ? cudaClusterSchedulingPolicySpread : cudaClusterSchedulingPolicyLoadBalancing;
+            ++na;
+        }
     }
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[na].val.programmaticStreamSerializationAllowed = 1;

@@ -44,14 +44,18 @@
 
 namespace lowm {
 
-constexpr int kTileN = 64;          // output columns per CTA = MMA M
+// Output columns per CTA (tile_n) = the MMA's M: 64 or 128, a template
+// parameter of the kernels.
 constexpr int kBlockK = 64;         // K elements per block (one 128-byte swizzle row of bf16)
 constexpr int kMmaK = 16;           // K per tcgen05.mma of kind::f16
 constexpr int kMaxKbPerStage = 8;   // K blocks per stage: 1, 2, 4 or 8
 constexpr int kThreads = 192;       // 6 warps
 constexpr int kEpilogueWarp0 = 2;   // warps 2..5; warp % 4 covers every TMEM lane quarter once
 constexpr int kEpilogueThreads = 128;
-constexpr uint32_t kWBlockBytes = kTileN * kBlockK * 2;   // 8 KiB per 64 x 64 W block
+__host__ __device__ constexpr uint32_t w_block_bytes(int tile_n)   // one tile_n x 64 W block
+{
+    return (uint32_t)tile_n * kBlockK * 2u;
+}
 constexpr uint32_t kTmemBarArrivals = 32 + kEpilogueThreads;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;     // 2 s per wait on another party
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;       // 2 s for this CTA's own copies / MMAs in flight
@@ -69,10 +73,9 @@ enum : uint32_t {
     kErrReduce = 1u << 8,
 };
 
-__device__ unsigned int g_lowm_status;   // read and cleared by lowm_gemm_sync_status
-
 struct KernelParams {
     __nv_bfloat16 *C;
+    unsigned int *status;   // device status word (bits of the waits that gave up), owned by the library
     int M, N, K;
     int stages;             // ring depth
     int kb_per_stage;       // 64-wide K blocks per stage (divides kb_per_rank)
@@ -97,19 +100,19 @@ struct SmemLayout {
 
 // `bufs` = 1 for the one-tile-per-cluster kernel, 2 for the persistent kernel
 // (double-buffered mailbox and output staging).
-__host__ __device__ inline SmemLayout make_smem_layout(int m_pad, int split_k, int stages, int kb_per_stage,
-                                                       int bufs = 1)
+__host__ __device__ inline SmemLayout make_smem_layout(int tile_n, int m_pad, int split_k, int stages,
+                                                       int kb_per_stage, int bufs = 1)
 {
     SmemLayout L;
     uint32_t off = 0;
-    L.w = off;                                            // [stages][kb_per_stage][64 n][64 k] bf16
-    off += (uint32_t)stages * (uint32_t)kb_per_stage * kWBlockBytes;
+    L.w = off;                                            // [stages][kb_per_stage][tile_n][64 k] bf16
+    off += (uint32_t)stages * (uint32_t)kb_per_stage * w_block_bytes(tile_n);
     L.a = off;                                            // [stages][kb_per_stage][m_pad][64 k]; m_pad*128 % 1024 == 0
     off += (uint32_t)stages * (uint32_t)kb_per_stage * (uint32_t)m_pad * 128u;
-    L.mailbox = off;                                      // [bufs][(split_k-1)][64 n][m_pad] fp32
-    off += (uint32_t)bufs * (uint32_t)(split_k - 1) * kTileN * (uint32_t)m_pad * 4u;
-    L.out = off;                                          // [bufs][m_pad][64 n] bf16 staging for C
-    off += (uint32_t)bufs * (uint32_t)m_pad * kTileN * 2u;
+    L.mailbox = off;                                      // [bufs][(split_k-1)][tile_n][m_pad] fp32
+    off += (uint32_t)bufs * (uint32_t)(split_k - 1) * (uint32_t)tile_n * (uint32_t)m_pad * 4u;
+    L.out = off;                                          // [bufs][m_pad][tile_n] bf16 staging for C
+    off += (uint32_t)bufs * (uint32_t)m_pad * (uint32_t)tile_n * 2u;
     L.bars = off;                                         // full[stages], empty[stages], then per-kernel barriers
     off += (uint32_t)(2 * stages + 12) * 8u;
     L.tmem_slot = off;
@@ -135,7 +138,7 @@ __device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t saddr)
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, shape M x N (M = 64 here, N = m_pad).
+// K-major, shape M x N (M = tile_n, N = m_pad).
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int mma_m, int mma_n)
 {
     return (1u << 4)                                      // D format: f32
@@ -150,14 +153,20 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int cols)
     return cols <= 32 ? 32u : (cols <= 64 ? 64u : (cols <= 128 ? 128u : (cols <= 256 ? 256u : 512u)));
 }
 
-// TMEM placement of the M = 64 (cta_group::1) accumulator: row i of D lives
-// in lane 32 * (i / 16) + i % 16, i.e. the first 16 lanes of each 32-lane
-// quarter.  An epilogue warp with quarter q therefore holds rows 16q..16q+15
-// in its threads 0..15.
+// TMEM placement of the cta_group::1 accumulator.  M = 128: row i of D lives
+// in lane i, so an epilogue warp with lane quarter q holds rows 32q..32q+31.
+// M = 64: row i lives in lane 32 * (i / 16) + i % 16 (the first 16 lanes of
+// each 32-lane quarter), so quarter q holds rows 16q..16q+15 in threads 0..15.
+template <int TILE_N>
 __device__ __forceinline__ bool tmem_row_of_thread(int quarter, int lane, int &row)
 {
-    row = 16 * quarter + lane;
-    return lane < 16;
+    if constexpr (TILE_N == 128) {
+        row = 32 * quarter + lane;
+        return true;
+    } else {
+        row = 16 * quarter + lane;
+        return lane < 16;
+    }
 }
 
 // Epilogue load of this warp's lane quarter: M_PAD fp32 columns, then
@@ -178,13 +187,13 @@ __device__ __forceinline__ void load_accumulator(uint32_t taddr, float (&acc)[M_
 
 // One stage's MMAs: kb_per_stage blocks x 4 K16 steps into the accumulator at
 // tmem_d.  `first` clears the accumulator with the stage's first MMA.
-template <int M_PAD>
+template <int TILE_N, int M_PAD>
 __device__ __forceinline__ void mma_stage(uint32_t tmem_d, uint32_t w_stage, uint32_t a_stage, int kb_per_stage,
                                           bool first)
 {
-    constexpr uint32_t kIdesc = make_idesc_bf16(kTileN, M_PAD);
+    constexpr uint32_t kIdesc = make_idesc_bf16(TILE_N, M_PAD);
     for (int j = 0; j < kb_per_stage; ++j) {
-        const uint64_t adesc = make_sw128_kmajor_desc(w_stage + (uint32_t)j * kWBlockBytes);
+        const uint64_t adesc = make_sw128_kmajor_desc(w_stage + (uint32_t)j * w_block_bytes(TILE_N));
         const uint64_t bdesc = make_sw128_kmajor_desc(a_stage + (uint32_t)j * (M_PAD * 128u));
 #pragma unroll
         for (int kk = 0; kk < kBlockK / kMmaK; ++kk)      // +32 bytes of K per step: +2 in the encoded address
@@ -210,17 +219,20 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     }
 }
 
-__device__ __forceinline__ void record_error(uint32_t bits)
+__device__ __forceinline__ void record_error(const KernelParams &p, uint32_t bits)
 {
-    atomicOr(&g_lowm_status, bits);
+    atomicOr(p.status, bits);
 }
 
-template <int M_PAD, int SPLIT_K>
+template <int TILE_N, int M_PAD, int SPLIT_K>
 __global__ void __launch_bounds__(kThreads, 1)
     lowm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                        const KernelParams p)
 {
-    static_assert(M_PAD % 8 == 0 && M_PAD >= 8 && M_PAD <= 64, "m_pad is the MMA N: 8..64 in steps of 8");
+    static_assert(TILE_N == 64 || TILE_N == 128, "tile_n is the MMA M");
+    static_assert(M_PAD % (TILE_N == 128 ? 16 : 8) == 0 && M_PAD >= 8 && M_PAD <= 64,
+                  "m_pad is the MMA N: a multiple of 8 (M = 64) or 16 (M = 128), at most 64");
+    constexpr int kTileN = TILE_N;
     static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
     constexpr uint32_t kTmemCols = tmem_cols_for(M_PAD);
     constexpr uint32_t kSlotBytes = kTileN * M_PAD * 4u;          // one rank's fp32 partial tile
@@ -228,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int kbs = p.kb_per_stage;
-    const SmemLayout L = make_smem_layout(M_PAD, SPLIT_K, p.stages, kbs);
+    const SmemLayout L = make_smem_layout(TILE_N, M_PAD, SPLIT_K, p.stages, kbs);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int stages = p.stages;
-    const uint32_t w_stage_bytes = (uint32_t)kbs * kWBlockBytes;
+    const uint32_t w_stage_bytes = (uint32_t)kbs * w_block_bytes(TILE_N);
     const uint32_t a_stage_bytes = (uint32_t)kbs * (M_PAD * 128u);
     const uint32_t stage_tx = w_stage_bytes + a_stage_bytes;
     const int n_stages = p.kb_per_rank / kbs;                     // stage iterations of this rank
@@ -299,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = i % stages;
                 const uint32_t ph = (uint32_t)(i / stages) & 1u;
                 if (!wait_bounded<false>(bar_empty + 8u * s, ph ^ 1u, p.timeout_ns)) {
-                    record_error(kErrProducerEmpty);
+                    record_error(p, kErrProducerEmpty);
                     break;
                 }
                 ptx::mbar_arrive_expect_tx(bar_full + 8u * s, stage_tx);
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the last load on each stage must have completed.
             for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
                 if (!wait_bounded<false>(bar_full + 8u * (j % stages), (uint32_t)(j / stages) & 1u, kDrainTimeoutNs)) {
-                    record_error(kErrProducerDrain);
+                    record_error(p, kErrProducerDrain);
                     break;
                 }
         }
@@ -335,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = i % stages;
                 const uint32_t ph = (uint32_t)(i / stages) & 1u;
                 if (!wait_bounded<false>(bar_full + 8u * s, ph, p.timeout_ns)) {
-                    record_error(kErrMmaFull);
+                    record_error(p, kErrMmaFull);
                     break;
                 }
                 if (p.timeline != nullptr && (i == 0 || i == n_stages - 1))
                     p.timeline[4 * blockIdx.x + (i == 0 ? 1 : 2)] = ptx::globaltimer();
                 ptx::tcgen05_fence_after_thread_sync();
-                mma_stage<M_PAD>(tmem_d, sbase + L.w + (uint32_t)s * w_stage_bytes,
+                mma_stage<TILE_N, M_PAD>(tmem_d, sbase + L.w + (uint32_t)s * w_stage_bytes,
                                  sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, i == 0);
                 ptx::tcgen05_commit(bar_empty + 8u * s);           // stage free once these MMAs have read it
             }
@@ -360,14 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 128 arrivals the epilogue makes after tcgen05.wait::ld, and the
         // parity-1 wait returns only when all of those have happened.
         if (!wait_bounded<false>(bar_tmem_alloc, 0, p.timeout_ns))
-            record_error(kErrMmaTmemPhase0);
+            record_error(p, kErrMmaTmemPhase0);
         ptx::mbar_arrive(bar_tmem_alloc);          // phase 1 (32 lanes)
         if (!wait_bounded<false>(bar_tmem_alloc, 1, p.timeout_ns))
-            record_error(kErrMmaTmemPhase1);
+            record_error(p, kErrMmaTmemPhase1);
         // Every MMA this CTA issued has completed before its columns are freed
         // (already implied on the normal path, where the epilogue waited for it).
         if (!wait_bounded<false>(bar_acc, 0, kDrainTimeoutNs))
-            record_error(kErrMmaAccDrain);
+            record_error(p, kErrMmaAccDrain);
         ptx::tcgen05_fence_after_thread_sync();
         if (p.probes != nullptr && lane == 0) {
             const uint64_t t = ptx::globaltimer();
@@ -388,12 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar_tmem_alloc);          // first arrival: phase 0
         bool ok = wait_bounded<false>(bar_tmem_alloc, 0, p.timeout_ns);
         if (!ok)
-            record_error(kErrEpiTmemPhase0);
+            record_error(p, kErrEpiTmemPhase0);
         ptx::tcgen05_fence_after_thread_sync();
         const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot);
         ptx::griddep_wait();                       // C may belong to the previous kernel in the stream
         if (ok && !wait_bounded<false>(bar_acc, 0, p.timeout_ns)) {
-            record_error(kErrEpiAccFull);
+            record_error(p, kErrEpiAccFull);
             ok = false;
         }
         ptx::tcgen05_fence_after_thread_sync();
@@ -419,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
 
         int row;
-        const bool valid = tmem_row_of_thread(quarter, lane, row);   // row = n within the tile
+        const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
         if (SPLIT_K > 1 && rank != 0) {
             // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
             if (ok && valid && !p.drop_mailbox) {
@@ -437,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Owner: relaxed cluster-scope observation of the mailbox phase,
                 // then one acquire fence restricted to shared::cluster memory.
                 if (!wait_bounded<true>(bar_reduce, 0, p.reduce_timeout_ns)) {
-                    record_error(kErrReduce);
+                    record_error(p, kErrReduce);
                     ok = false;
                 }
                 ptx::fence_acquire_shared_cluster();
@@ -471,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ptx::named_barrier_sync(1, kEpilogueThreads);
-            // 16-byte coalesced stores: row m of the tile is 64 bf16 = 8 chunks.
+            // 16-byte coalesced stores: row m of the tile is tile_n bf16 = tile_n / 8 chunks.
             for (int c = etid; c < p.M * (kTileN / 8); c += kEpilogueThreads) {
-                const int m = c >> 3, ch = c & 7;
+                const int m = c / (kTileN / 8), ch = c % (kTileN / 8);   // 16-byte chunk ch of row m
                 const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
                 *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
             }
@@ -481,33 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
         }
     }
-}
-
-// The concurrent TMEM allocator of the stress method: allocate, fill with NaN,
-// free.  128 threads; never waits on another kernel.
-__global__ void __launch_bounds__(128) tmem_hog_kernel(int ncols, int iters)
-{
-    __shared__ uint32_t slot;
-    const int warp = threadIdx.x >> 5;
-    if (warp == 0) {
-        ptx::tmem_alloc(ptx::smem_u32(&slot), (uint32_t)ncols);
-        ptx::tmem_relinquish_alloc_permit();
-    }
-    ptx::tcgen05_fence_before_thread_sync();
-    __syncthreads();
-    ptx::tcgen05_fence_after_thread_sync();
-    const uint32_t base = slot + ((uint32_t)(32 * warp) << 16);
-    const uint32_t nan8[8] = {0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u,
-                              0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u};
-    for (int it = 0; it < iters; ++it)
-        for (int c = 0; c < ncols; c += 8)
-            ptx::tmem_st_32x32b_x8(base + (uint32_t)c, nan8);
-    ptx::tmem_wait_st();
-    ptx::tcgen05_fence_before_thread_sync();
-    __syncthreads();
-    ptx::tcgen05_fence_after_thread_sync();
-    if (warp == 0)
-        ptx::tmem_dealloc(slot, (uint32_t)ncols);
 }
 
 }  // namespace lowm

@@ -1,0 +1,20 @@
+// Internal interface between the host launcher and the kernel instances,
+// which are compiled in separate translation units (one per tile width) so
+// the library builds in parallel.
+#pragma once
+
+#include <cuda.h>
+
+#include "lowm_kernel.cuh"
+
+namespace lowm {
+
+typedef void (*KernelFn)(CUtensorMap, CUtensorMap, KernelParams);
+
+// The kernel for (m_pad, split_k, persistent) at 64-column tiles (m_pad 8, 16,
+// 32, 64) and at 128-column tiles (m_pad 16, 32, 64); nullptr when no
+// instance exists.
+KernelFn kernel_tile64(int m_pad, int split_k, bool persistent);
+KernelFn kernel_tile128(int m_pad, int split_k, bool persistent);
+
+}  // namespace lowm

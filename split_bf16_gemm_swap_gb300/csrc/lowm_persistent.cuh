@@ -27,12 +27,15 @@
 
 namespace lowm {
 
-template <int M_PAD, int SPLIT_K>
+template <int TILE_N, int M_PAD, int SPLIT_K>
 __global__ void __launch_bounds__(kThreads, 1)
     lowm_splitk_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                   const __grid_constant__ CUtensorMap tmap_w, const KernelParams p)
 {
-    static_assert(M_PAD % 8 == 0 && M_PAD >= 8 && M_PAD <= 64, "m_pad is the MMA N: 8..64 in steps of 8");
+    static_assert(TILE_N == 64 || TILE_N == 128, "tile_n is the MMA M");
+    static_assert(M_PAD % (TILE_N == 128 ? 16 : 8) == 0 && M_PAD >= 8 && M_PAD <= 64,
+                  "m_pad is the MMA N: a multiple of 8 (M = 64) or 16 (M = 128), at most 64");
+    constexpr int kTileN = TILE_N;
     static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
     constexpr uint32_t kBufCols = M_PAD;                          // one tile's accumulator
     constexpr uint32_t kTmemCols = tmem_cols_for(2 * kBufCols);
@@ -43,10 +46,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int kbs = p.kb_per_stage;
-    const SmemLayout L = make_smem_layout(M_PAD, SPLIT_K, p.stages, kbs, 2);
+    const SmemLayout L = make_smem_layout(TILE_N, M_PAD, SPLIT_K, p.stages, kbs, 2);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int stages = p.stages;
-    const uint32_t w_stage_bytes = (uint32_t)kbs * kWBlockBytes;
+    const uint32_t w_stage_bytes = (uint32_t)kbs * w_block_bytes(TILE_N);
     const uint32_t a_stage_bytes = (uint32_t)kbs * (M_PAD * 128u);
     const uint32_t stage_tx = w_stage_bytes + a_stage_bytes;
     const int warp = threadIdx.x >> 5;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = i % stages;
                 const uint32_t ph = (uint32_t)(i / stages) & 1u;
                 if (!wait_bounded<false>(bar_empty + 8u * s, ph ^ 1u, p.timeout_ns)) {
-                    record_error(kErrProducerEmpty);
+                    record_error(p, kErrProducerEmpty);
                     break;
                 }
                 const int n0 = (cluster + (i / spt) * clusters) * kTileN;
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::griddep_launch_dependents();
             for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
                 if (!wait_bounded<false>(bar_full + 8u * (j % stages), (uint32_t)(j / stages) & 1u, kDrainTimeoutNs)) {
-                    record_error(kErrProducerDrain);
+                    record_error(p, kErrProducerDrain);
                     break;
                 }
         }
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t u = (uint32_t)(j >> 1);
                 // The epilogue must have read this buffer's previous tile.
                 if (!wait_bounded<false>(bar_acc_empty + 8u * b, (u & 1u) ^ 1u, p.timeout_ns)) {
-                    record_error(kErrMmaFull);
+                    record_error(p, kErrMmaFull);
                     break;
                 }
                 ptx::tcgen05_fence_after_thread_sync();
@@ -168,14 +171,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s = i % stages;
                     const uint32_t ph = (uint32_t)(i / stages) & 1u;
                     if (!wait_bounded<false>(bar_full + 8u * s, ph, p.timeout_ns)) {
-                        record_error(kErrMmaFull);
+                        record_error(p, kErrMmaFull);
                         ok = false;
                         break;
                     }
                     if (p.timeline != nullptr && (i == 0 || i == my_tiles * spt - 1))
                         p.timeline[4 * blockIdx.x + (i == 0 ? 1 : 2)] = ptx::globaltimer();
                     ptx::tcgen05_fence_after_thread_sync();
-                    mma_stage<M_PAD>(d, sbase + L.w + (uint32_t)s * w_stage_bytes,
+                    mma_stage<TILE_N, M_PAD>(d, sbase + L.w + (uint32_t)s * w_stage_bytes,
                                      sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, st == 0);
                     ptx::tcgen05_commit(bar_empty + 8u * s);
                 }
@@ -190,15 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // second arrival, so phase 1 = its second arrivals plus the epilogue's
         // arrivals made after its final tcgen05.wait::ld).
         if (!wait_bounded<false>(bar_tmem_alloc, 0, p.timeout_ns))
-            record_error(kErrMmaTmemPhase0);
+            record_error(p, kErrMmaTmemPhase0);
         ptx::mbar_arrive(bar_tmem_alloc);
         if (!wait_bounded<false>(bar_tmem_alloc, 1, p.timeout_ns))
-            record_error(kErrMmaTmemPhase1);
+            record_error(p, kErrMmaTmemPhase1);
         // Every MMA this CTA issued has completed: the last commit on each buffer.
         for (int b = 0; b < 2 && b < my_tiles; ++b) {
             const int last = my_tiles - 1 - ((my_tiles - 1 - b) & 1);   // last tile index with parity b
             if (!wait_bounded<false>(bar_acc_full + 8u * b, (uint32_t)(last >> 1) & 1u, kDrainTimeoutNs))
-                record_error(kErrMmaAccDrain);
+                record_error(p, kErrMmaAccDrain);
         }
         ptx::tcgen05_fence_after_thread_sync();
         if (p.probes != nullptr && lane == 0) {
@@ -220,12 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar_tmem_alloc);          // first arrival: phase 0
         bool ok = wait_bounded<false>(bar_tmem_alloc, 0, p.timeout_ns);
         if (!ok)
-            record_error(kErrEpiTmemPhase0);
+            record_error(p, kErrEpiTmemPhase0);
         ptx::tcgen05_fence_after_thread_sync();
         const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot);
         ptx::griddep_wait();
         int row;
-        const bool valid = tmem_row_of_thread(quarter, lane, row);
+        const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);
         unsigned long long t_ld = 0;
 
         for (int j = 0; j < my_tiles; ++j) {
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t u = (uint32_t)(j >> 1);
             const int n0 = (cluster + j * clusters) * kTileN;
             if (ok && !wait_bounded<false>(bar_acc_full + 8u * b, u & 1u, p.timeout_ns)) {
-                record_error(kErrEpiAccFull);
+                record_error(p, kErrEpiAccFull);
                 ok = false;
             }
             ptx::tcgen05_fence_after_thread_sync();
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Wait until the owner has consumed this mailbox buffer's previous tile.
                 bool free_ok = wait_bounded<true>(bar_mbox_free + 8u * b, (u & 1u) ^ 1u, p.timeout_ns);
                 if (!free_ok)
-                    record_error(kErrReduce);
+                    record_error(p, kErrReduce);
                 ptx::fence_acquire_shared_cluster();
                 if (ok && free_ok && valid && !p.drop_mailbox) {
                     const uint32_t dst = ptx::mapa_shared(
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool red_ok = true;
                 if (SPLIT_K > 1) {
                     if (!wait_bounded<true>(bar_reduce + 8u * b, u & 1u, p.reduce_timeout_ns)) {
-                        record_error(kErrReduce);
+                        record_error(p, kErrReduce);
                         red_ok = false;
                     }
                     ptx::fence_acquire_shared_cluster();
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mbar_arrive_remote_release_cluster(ptx::mapa_shared(bar_mbox_free + 8u * b, (uint32_t)r));
                 }
                 for (int c = etid; c < p.M * (kTileN / 8); c += kEpilogueThreads) {
-                    const int m = c >> 3, ch = c & 7;
+                    const int m = c / (kTileN / 8), ch = c % (kTileN / 8);   // 16-byte chunk ch of row m
                     const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
                     *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
                 }

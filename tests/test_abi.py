@@ -46,21 +46,39 @@ def test_status_strings(L):
     assert "unknown" in lowm.status_string(99)
 
 
-def test_shipped_tactic_is_reproduced(L):
+def test_shipped_tactic_is_reproduced(L, monkeypatch):
+    # The pages' tactic (64, 8, 2, 10): 64-column tiles, m_pad 8, split_k 2, 10
+    # single-block stages.
+    monkeypatch.setenv("LOWM_TILE_N", "64")
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", "1")
+    monkeypatch.setenv("LOWM_STAGES", "10")
     st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
     assert st == lowm.LOWM_OK
-    assert (t["tile_n"], t["m_pad"], t["split_k"], t["block_k"]) == (64, 8, 2, 64)
+    assert (t["tile_n"], t["m_pad"], t["split_k"], t["stages"], t["block_k"]) == (64, 8, 2, 10, 64)
     assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["pdl"] == 1 and t["persistent"] == 0
-    assert t["stages"] * t["kb_per_stage"] >= 8 and t["smem_bytes"] <= 232448
-    assert t["kb_per_stage"] == 4          # 32 blocks per rank: 4 per 3-D copy
+
+
+def test_default_tactic_for_the_headline_workload(L):
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK
+    assert (t["tile_n"], t["m_pad"], t["split_k"], t["kb_per_stage"], t["stages"]) == (64, 8, 2, 4, 3)
+    assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["persistent"] == 0 and t["smem_bytes"] <= 232448
+
+
+@pytest.mark.parametrize("M,tile", [(4, 64), (16, 64), (17, 128), (32, 128), (64, 128)])
+def test_tile_width_follows_m_pad(L, M, tile):
+    st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and t["tile_n"] == tile
 
 
 @pytest.mark.parametrize("M,N,K,sk", [(4, 2304, 12288, 4), (4, 49152, 4096, 2), (16, 6144, 32768, 4),
                                       (64, 6144, 4096, 1), (4, 6144, 4096, 2)])
 def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
-    assert st == lowm.LOWM_OK and t["split_k"] == sk and t["tiles"] == N // 64
-    assert t["m_pad"] == (8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64)
+    assert st == lowm.LOWM_OK and t["split_k"] == sk and t["tiles"] == N // t["tile_n"]
+    assert t["tile_n"] in (64, 128)
+    mp = 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
+    assert t["m_pad"] == (max(mp, 16) if t["tile_n"] == 128 else mp)
     assert t["ctas"] == t["num_clusters"] * sk
     if t["persistent"]:
         # every cluster gets ceil(tiles / clusters) tiles and none is idle
@@ -71,12 +89,13 @@ def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
 
 
 @pytest.mark.parametrize("M,N,K,sk,kbs,stages", [
-    # the ring each workload measured fastest with on GB300 (tactic sweep)
+    # the 64-column ring each workload measured fastest with on GB300 (tactic sweep)
     (4, 6144, 4096, 2, 4, 3), (4, 2304, 12288, 4, 8, 2), (4, 49152, 4096, 2, 2, 2), (4, 49152, 4096, 1, 4, 2),
     (16, 6144, 32768, 4, 2, 2)])
-def test_ring_matches_the_measured_best(L, M, N, K, sk, kbs, stages):
+def test_ring_matches_the_measured_best(L, M, N, K, sk, kbs, stages, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "64")
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
-    assert st == lowm.LOWM_OK and (t["kb_per_stage"], t["stages"]) == (kbs, stages)
+    assert st == lowm.LOWM_OK and (t["tile_n"], t["kb_per_stage"], t["stages"]) == (64, kbs, stages)
 
 
 @pytest.mark.parametrize("M,N,K,sk", [(4, 256, 64 * 3, 1), (4, 256, 64 * 6, 1), (4, 256, 64 * 5, 1),
@@ -100,6 +119,7 @@ def test_kb_per_stage_override(L, monkeypatch):
 
 
 def test_persistent_override_and_cap(L, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "64")
     monkeypatch.setenv("LOWM_PERSISTENT", "1")
     monkeypatch.setenv("LOWM_MAX_CLUSTERS", "4")
     st, t = lowm.lowm_gemm_query_tactic(4, 13 * 64, 1024, 2)

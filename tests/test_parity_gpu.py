@@ -333,3 +333,62 @@ def test_persistent_with_kb_per_stage(kbs, monkeypatch):
     monkeypatch.setenv("LOWM_MAX_CLUSTERS", "5")
     A, W = inputs.make_problem(4, 17 * 64, 2048, seed=10)
     check(A, W, 2)
+
+
+# ---------------------------------------------------------------- 128-column tiles (MMA M = 128)
+def test_identity_weight_maps_every_column_tile128(monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "128")
+    M, N, K = 8, 128, 256
+    A = (torch.arange(M * K, dtype=torch.float32).reshape(M, K) % 251 + 1).to(torch.bfloat16)
+    W = torch.zeros((N, K), dtype=torch.bfloat16)
+    W[torch.arange(N), torch.arange(N)] = 1.0
+    for split_k in (1, 2):
+        st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+        assert st == lowm.LOWM_OK and t["tile_n"] == 128
+        C, _ = run_gpu(A, W, split_k, want_f32=False)
+        want = inputs.bits(A)[:, :N]
+        if not np.array_equal(C, want):
+            vals = {int(v): i for i, v in enumerate(want[0])}
+            got_cols = [vals.get(int(v), -1) for v in C[0]]
+            raise AssertionError("split_k %d: output column n holds input column %s" % (split_k, got_cols))
+
+
+TILE128 = [
+    (1, 128, 256, 1), (4, 384, 1024, 2), (13, 256, 2048, 4), (16, 128, 4096, 8), (17, 256, 512, 2),
+    (32, 384, 1024, 1), (33, 128, 768, 2), (64, 256, 2048, 4), (4, 6144, 4096, 2), (8, 1280, 64 * 12, 4),
+]
+
+
+@pytest.mark.parametrize("M,N,K,split_k", TILE128)
+def test_tile128_random(M, N, K, split_k, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "128")
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK
+    A, W = inputs.make_problem(M, N, K, seed=700 + M + N + K)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(16, 6144, 32768, 4), (4, 256, 4096, 2), (64, 128, 1024, 1)])
+def test_tile128_integer_exact(M, N, K, split_k, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "128")
+    A, W = inputs.make_problem(M, N, K, seed=11, kind="int")
+    check(A, W, split_k, exact=True)
+
+
+def test_tile128_persistent(monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "128")
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", "3")
+    st, t = lowm.lowm_gemm_query_tactic(4, 11 * 128, 2048, 2)
+    assert st == lowm.LOWM_OK and t["tile_n"] == 128 and t["persistent"] == 1
+    A, W = inputs.make_problem(4, 11 * 128, 2048, seed=12)
+    check(A, W, 2)
+
+
+def test_tile64_and_tile128_agree_within_tolerance(monkeypatch):
+    A, W = inputs.make_problem(4, 1024, 4096, seed=13)
+    monkeypatch.setenv("LOWM_TILE_N", "64")
+    C64 = check(A, W, 2)
+    monkeypatch.setenv("LOWM_TILE_N", "128")
+    C128 = check(A, W, 2)
+    assert C64.shape == C128.shape                      # both met the parity bar inside check()
