@@ -179,6 +179,7 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
  *                    tcgen05.dealloc.  Zero-initialise before the launch.
  *   c_f32            NULL, or device float[M*N]: the fp32 sums before the bf16
  *                    rounding (written by the owner rank)
+ *   flags            launch flags as for lowm_gemm_bf16_ex (LOWM_FLAG_*)
  *   timeline         NULL, or device u64[4 * ctas]: per CTA, %globaltimer at
  *                    [0] the end of the prologue, [1] the MMA warp's first
  *                    full stage, [2] its last full stage, [3] the end of the
@@ -195,6 +196,7 @@ typedef struct {
     unsigned long long *probes;
     float *c_f32;
     unsigned long long *timeline;
+    unsigned int flags;
 } lowm_debug_opts_t;
 
 /* lowm_gemm_bf16 with the hooks above (opts may be NULL: same as lowm_gemm_bf16). */

@@ -317,17 +317,18 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         return LOWM_ERR_INVALID_ARGUMENT;
     const int nsm = sms > 0 ? sms : 152;
     // Tile width.  128-column tiles (MMA M = 128: every epilogue lane holds a
-    // row, and each W copy is twice as large) measured faster for m_pad >= 32
-    // (M4..64 sweep at N6144 K4096); for m_pad 8 and 16, 64-column tiles
-    // were as fast or faster.  LOWM_TILE_N = 64 / 128 overrides when the shape
-    // allows it (tuning).
+    // row, and each W copy is twice as large) measured faster for m_pad 16
+    // and 64 and slower for m_pad 8 and 32 (M 8..64 sweep at N6144 K4096 and
+    // M16 N6144 K32768 on GB300).  LOWM_TILE_N = 64 / 128 overrides when the
+    // shape allows it (tuning).
     int tile_n = 64;
     {
         const int force = env_int("LOWM_TILE_N", 0);
         const bool can128 = N % 128 == 0;
+        const int mp = m_pad_of(M);
         if (force == 128 && can128)
             tile_n = 128;
-        else if (force != 64 && can128 && m_pad_of(M) >= 32)
+        else if (force != 64 && can128 && (mp == 16 || mp == 64))
             tile_n = 128;
     }
     int m_pad = m_pad_of(M);
@@ -583,7 +584,7 @@ lowm_status_t lowm_gemm_bf16_ex(const void *A, const void *W, void *C, int M, in
 lowm_status_t lowm_gemm_bf16_debug(const void *A, const void *W, void *C, int M, int N, int K, int split_k,
                                    void *stream, const lowm_debug_opts_t *opts)
 {
-    return launch(A, W, C, M, N, K, split_k, stream, opts);
+    return launch(A, W, C, M, N, K, split_k, stream, opts, opts ? opts->flags : 0u);
 }
 
 lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tactic_t *out)

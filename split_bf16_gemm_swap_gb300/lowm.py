@@ -59,6 +59,7 @@ class lowm_debug_opts_t(ctypes.Structure):
         ("probes", ctypes.c_void_p),
         ("c_f32", ctypes.c_void_p),
         ("timeline", ctypes.c_void_p),
+        ("flags", ctypes.c_uint),
     ]
 
 
@@ -155,9 +156,10 @@ def lowm_gemm_bf16_host(A_host, W_host, C_host, A_dev, W_dev, C_dev, M, N, K, sp
 
 def lowm_gemm_bf16_debug(A, W, C, M, N, K, split_k=0, stream=None, *, stall_warp_mask=0, stall_rank_mask=0,
                          stall_ns=0, full_smem=0, stages=0, drop_mailbox=0, reduce_timeout_ns=0, probes=None,
-                         c_f32=None, timeline=None) -> int:
+                         c_f32=None, timeline=None, flags=0) -> int:
     o = lowm_debug_opts_t(int(stall_warp_mask), int(stall_rank_mask), int(stall_ns), int(full_smem), int(stages),
-                          int(drop_mailbox), int(reduce_timeout_ns), _ptr(probes), _ptr(c_f32), _ptr(timeline))
+                          int(drop_mailbox), int(reduce_timeout_ns), _ptr(probes), _ptr(c_f32), _ptr(timeline),
+                          int(flags))
     return lib().lowm_gemm_bf16_debug(_ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K), int(split_k),
                                       _stream(stream), ctypes.byref(o))
 

@@ -71,6 +71,7 @@ CONFIGS = [
     (4, 6144, 4096, 2, "randn"),
     (4, 2304, 12288, 4, "randn"),
     (4, 49152, 4096, 2, "randn"),
+    (64, 6144, 4096, 2, "randn"),          # 128-column tiles (MMA M = 128)
 ]
 
 
@@ -108,5 +109,27 @@ def test_stalling_only_one_rank(stall_rank_mask):
     ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
     assert lowm.lowm_gemm_bf16(Ad, Wd, ref, M, N, K, split_k, None) == lowm.LOWM_OK
     outs, probes = stressed(Ad, Wd, M, N, K, split_k, 10_000, hog_cols=32, stall_rank_mask=stall_rank_mask)
+    assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
+    check_probes(probes)
+
+
+@pytest.mark.parametrize("tile", ["64", "128"])
+def test_persistent_schedule_under_stress(tile, monkeypatch):
+    # Several tiles per cluster: the TMEM release after the last tile and the
+    # double-buffered mailbox hand-off, under the same stall + hog method.
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", "16")
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    M, N, K, split_k = 16, 6144, 8192, 2
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK and t["persistent"] == 1 and t["tiles_per_cluster"] >= 3
+    A, W = inputs.make_problem(M, N, K, seed=1234, kind="int")
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16(Ad, Wd, ref, M, N, K, split_k, None) == lowm.LOWM_OK
+    torch.cuda.synchronize()
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(inputs.bits(ref.cpu()), np.broadcast_to(inputs.bits(col[None, :]), (M, N)))
+    outs, probes = stressed(Ad, Wd, M, N, K, split_k, 10_000)
     assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
     check_probes(probes)
