@@ -64,7 +64,7 @@ typedef enum {
  *   split_k      CTAs per cluster along K (1, 2, 4 or 8)
  *   stages       depth of the shared-memory ring between the TMA producer and the MMA warp
  *   block_k      K elements per block (64: one 128-byte swizzle row of bf16)
- *   tiles        N / tile_n output tiles
+ *   tiles        ceil(N / tile_n) output tiles (the last may be partial)
  *   num_clusters clusters launched: `tiles` (one tile each), or fewer when
  *                persistent
  *   ctas         num_clusters * split_k
@@ -92,7 +92,10 @@ typedef struct {
 /*
  * C = A . W^T on `stream`.
  *   M        1..64
- *   N        a positive multiple of 64
+ *   N        any positive value; when N is not a multiple of tile_n the last
+ *            tile is partial (the TMA unit zero-fills W rows >= N and the
+ *            epilogue stores only columns < N; 16-byte stores when N % 8 == 0,
+ *            element stores otherwise)
  *   K        a positive multiple of split_k * 64
  *   split_k  0 (let the tactic table choose), 1, 2, 4 or 8
  *   A, W, C  device pointers, 16-byte aligned; C must not overlap A or W

@@ -2,7 +2,7 @@
 // table, TMA descriptor encoding (cached), and the cluster + PDL launch.
 //
 // Launch shape ("Fix two synchronization gaps in the MiniMax M3 low-M split-K
-// GEMM", TensorRT-LLM PR, Hardware verification): N / 64 clusters of split_k
+// GEMM", TensorRT-LLM PR, Hardware verification): ceil(N / 64) clusters of split_k
 // CTAs, programmatic dependent launch on, cluster dimension split_k along grid
 // x.  The host also guarantees the non-empty K loop that the PR's analysis of
 // the TMEM race relies on (Description, item 1): K must be a positive
@@ -188,7 +188,7 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, 
 
 bool shape_ok(int M, int N, int K, int split_k)
 {
-    return M >= 1 && M <= 64 && N > 0 && N % 64 == 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
+    return M >= 1 && M <= 64 && N > 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
 }
 
 // split_k = 0: the smallest split (1, 2, 4, 8) that keeps the K loop non-empty
@@ -197,7 +197,7 @@ bool shape_ok(int M, int N, int K, int split_k)
 int choose_split_k(int M, int N, int K, int sms)
 {
     (void)M;
-    const int tiles = N / 64;
+    const int tiles = (N + 63) / 64;
     int best = 0;
     for (int sk = 1; sk <= 8; sk *= 2) {
         if (K % (sk * lowm::kBlockK) != 0)
@@ -326,7 +326,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         const int force = env_int("LOWM_TILE_N", 0);
         const bool can128 = N % 128 == 0;
         const int mp = m_pad_of(M);
-        if (force == 128 && can128)
+        if (force == 128 && N >= 128)
             tile_n = 128;
         else if (force != 64 && can128 && (mp == 16 || mp == 64))
             tile_n = 128;
@@ -336,7 +336,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         m_pad = 16;                                     // MMA M = 128 needs N a multiple of 16
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1).
     bool persistent = env_int("LOWM_PERSISTENT", 0) == 1;
-    int tiles = N / tile_n;
+    int tiles = (N + tile_n - 1) / tile_n;            // the last tile may be partial
     int clusters = tiles;
     Ring ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
     if (stages_override >= 2)
@@ -346,7 +346,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         // e.g. m_pad 64 with split_k 8: the 128-column mailbox does not fit; use 64 columns
         tile_n = 64;
         m_pad = m_pad_of(M);
-        tiles = N / tile_n;
+        tiles = (N + tile_n - 1) / tile_n;
         clusters = tiles;
         ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
         if (stages_override >= 2)
@@ -614,7 +614,7 @@ const char *lowm_status_string(lowm_status_t s)
     switch (s) {
     case LOWM_OK: return "ok";
     case LOWM_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=64, N%64==0, K%(split_k*64)==0)";
+    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=64, N>=1, K%(split_k*64)==0)";
     case LOWM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case LOWM_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103 (GB300)";
     case LOWM_ERR_CUDA: return "CUDA runtime error";

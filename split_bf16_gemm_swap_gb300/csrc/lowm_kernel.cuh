@@ -478,16 +478,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.c_f32 != nullptr) {
 #pragma unroll
                     for (int m = 0; m < M_PAD; ++m)
-                        if (m < p.M)
+                        if (m < p.M && n0 + row < p.N)
                             p.c_f32[(size_t)m * p.N + n0 + row] = acc[m];
                 }
             }
             ptx::named_barrier_sync(1, kEpilogueThreads);
-            // 16-byte coalesced stores: row m of the tile is tile_n bf16 = tile_n / 8 chunks.
-            for (int c = etid; c < p.M * (kTileN / 8); c += kEpilogueThreads) {
-                const int m = c / (kTileN / 8), ch = c % (kTileN / 8);   // 16-byte chunk ch of row m
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
-                *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
+            if ((p.N & 7) == 0) {
+                // 16-byte coalesced stores: row m of the tile is tile_n bf16 = tile_n / 8
+                // chunks; a partial last tile stores only the chunks below N.
+                for (int c = etid; c < p.M * (kTileN / 8); c += kEpilogueThreads) {
+                    const int m = c / (kTileN / 8), ch = c % (kTileN / 8);   // 16-byte chunk ch of row m
+                    if (n0 + ch * 8 < p.N) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
+                        *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
+                    }
+                }
+            } else {
+                // N not a multiple of 8: rows of C are not 16-byte aligned; store elements.
+                for (int e = etid; e < p.M * kTileN; e += kEpilogueThreads) {
+                    const int m = e / kTileN, col = e % kTileN;
+                    if (n0 + col < p.N)
+                        p.C[(size_t)m * p.N + n0 + col] = stage_out[m * kTileN + col];
+                }
             }
             if (p.timeline != nullptr && etid == 0)
                 p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();

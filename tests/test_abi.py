@@ -75,7 +75,7 @@ def test_tile_width_follows_m_pad(L, M, tile):
                                       (64, 6144, 4096, 1), (4, 6144, 4096, 2)])
 def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
-    assert st == lowm.LOWM_OK and t["split_k"] == sk and t["tiles"] == N // t["tile_n"]
+    assert st == lowm.LOWM_OK and t["split_k"] == sk and t["tiles"] == -(-N // t["tile_n"])
     assert t["tile_n"] in (64, 128)
     mp = 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
     assert t["m_pad"] == (max(mp, 16) if t["tile_n"] == 128 else mp)
@@ -130,6 +130,17 @@ def test_persistent_override_and_cap(L, monkeypatch):
     assert st == lowm.LOWM_OK and t["persistent"] == 0 and t["ctas"] == 1536
 
 
+@pytest.mark.parametrize("M,N,K,sk", [(4, 1, 256, 1), (4, 72, 1024, 2), (16, 6150, 1024, 2), (1, 4095, 256, 1),
+                                      (64, 136, 1024, 2)])
+def test_any_n_is_tiled_with_a_partial_last_tile(L, M, N, K, sk):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    assert st == lowm.LOWM_OK
+    tn = t["tile_n"]
+    assert t["tiles"] == -(-N // tn) and (t["tiles"] - 1) * tn < N <= t["tiles"] * tn
+    if N % 128:
+        assert tn == 64          # 128-column tiles only where they divide N (unless forced)
+
+
 def test_auto_split_k_keeps_the_k_loop_non_empty(L):
     for M, N, K in [(4, 64, 64), (4, 64, 128), (4, 6144, 4096), (64, 64, 512), (1, 49152, 4096)]:
         st, t = lowm.lowm_gemm_query_tactic(M, N, K, 0)
@@ -140,7 +151,6 @@ def test_auto_split_k_keeps_the_k_loop_non_empty(L):
 @pytest.mark.parametrize("M,N,K,sk,want", [
     (0, 64, 64, 1, lowm.LOWM_ERR_INVALID_ARGUMENT),
     (65, 64, 64, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),
-    (4, 96, 64, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # N not a multiple of 64
     (4, 64, 96, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # K not a multiple of 64
     (4, 64, 64, 2, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # empty K loop on one rank
     (4, 64, 128, 3, lowm.LOWM_ERR_INVALID_ARGUMENT),      # split_k not a power of two

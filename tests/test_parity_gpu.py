@@ -392,3 +392,63 @@ def test_tile64_and_tile128_agree_within_tolerance(monkeypatch):
     monkeypatch.setenv("LOWM_TILE_N", "128")
     C128 = check(A, W, 2)
     assert C64.shape == C128.shape                      # both met the parity bar inside check()
+
+
+# ---------------------------------------------------------------- N not a multiple of the tile width
+NTAIL = [
+    # M, N, K, split_k: a partial last tile, with N % 8 == 0 (16-byte stores) and N % 8 != 0 (element stores)
+    (4, 1, 256, 1), (3, 8, 512, 2), (4, 72, 1024, 2), (5, 100, 512, 1), (8, 200, 2048, 4),
+    (16, 6152, 1024, 2), (16, 6150, 1024, 2), (33, 130, 512, 1), (64, 136, 1024, 2), (1, 4095, 256, 1),
+]
+
+
+@pytest.mark.parametrize("M,N,K,split_k", NTAIL)
+def test_n_tail_random(M, N, K, split_k):
+    A, W = inputs.make_problem(M, N, K, seed=500 + M + N)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("N", [72, 100, 6150])
+def test_n_tail_writes_nothing_past_n(N):
+    # C is the head of a larger buffer: the elements after C[M-1, N-1] must keep their sentinel.
+    M, K = 5, 1024
+    A, W = inputs.make_problem(M, N, K, seed=31)
+    flat = torch.full((M * N + 512,), 7.0, dtype=torch.bfloat16, device=DEV)
+    C = flat[:M * N].view(M, N)
+    F = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    assert lowm.lowm_gemm_bf16_debug(A.to(DEV), W.to(DEV), C, M, N, K, 2, None, c_f32=F) == lowm.LOWM_OK
+    sync_ok()
+    assert torch.all(flat[M * N:] == 7.0)
+    Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+    bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, bound)
+
+
+@pytest.mark.parametrize("tile", ["64", "128"])
+def test_n_tail_integer_exact(tile, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    M, N, K = 16, 6150, 4096
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, 2)
+    assert st == lowm.LOWM_OK and t["tile_n"] == int(tile) and t["tiles"] == -(-N // int(tile))
+    A, W = inputs.make_problem(M, N, K, seed=9, kind="int")
+    C = check(A, W, 2, exact=True)
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(C, np.broadcast_to(inputs.bits(col[None, :]), C.shape))
+
+
+@pytest.mark.parametrize("tile", ["64", "128"])
+def test_n_tail_persistent(tile, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    monkeypatch.setenv("LOWM_MAX_CLUSTERS", "3")
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    M, N, K = 16, 10 * 128 + 40, 2048
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, 2)
+    assert st == lowm.LOWM_OK and t["persistent"] == 1 and t["tiles_per_cluster"] >= 2
+    A, W = inputs.make_problem(M, N, K, seed=14)
+    check(A, W, 2)
+
+
+def test_largest_k_and_split():
+    # K = 65536 (the oracle's exact accumulator bound) over a cluster of 8.
+    A, W = inputs.make_problem(4, 256, 65536, seed=15)
+    check(A, W, 8)
