@@ -80,6 +80,15 @@ typedef enum {
  *                copy of W and one of A (the largest of 4, 2, 1 dividing the
  *                rank's block count): a copy has a fixed per-CTA cost, so
  *                larger copies are what let one CTA stream its share of HBM
+ *   mma_issuers  threads issuing tcgen05.mma per CTA: 2 for the one-tile
+ *                kernel (one takes the even, the other the odd 16-wide K steps
+ *                of every stage, each into its own TMEM accumulator; the
+ *                epilogue adds accumulator 0 + accumulator 1), 1 for the
+ *                persistent kernel.  One thread issues an MMA only every ~55
+ *                cycles, so at small m_pad the issuer paces the stream.
+ *   w_prefetch_stages  ring stages of W requested before the
+ *                programmatic-dependency wait under
+ *                LOWM_FLAG_W_BEFORE_PDL_WAIT (0 without the flag)
  * The pages' shipped tactic reads as (tile_n 64, m_pad 8, split_k 2, stages 10)
  * ("Fix two synchronization gaps ...", Hardware verification).
  */
@@ -87,6 +96,7 @@ typedef struct {
     int tile_n, m_pad, split_k, stages, block_k;
     int tiles, num_clusters, ctas, smem_bytes, pdl;
     int persistent, tiles_per_cluster, kb_per_stage;
+    int mma_issuers, w_prefetch_stages;
 } lowm_tactic_t;
 
 /*

@@ -261,7 +261,8 @@ lowm_status_t prepare_kernel(KernelFn fn)
 // arithmetic (shared memory and threads).
 int resident_clusters(int tile_n, int m_pad, int split_k, int smem, int sms, bool persistent, bool have_device)
 {
-    const int per_sm = std::min(kSmemPerSm / (smem + kSmemReservedPerCta), 2048 / lowm::kThreads);
+    const int threads = persistent ? lowm::kThreadsPersistent : lowm::kThreads;
+    const int per_sm = std::min(kSmemPerSm / (smem + kSmemReservedPerCta), 2048 / threads);
     const int formula = sms * per_sm / split_k;
     if (!have_device)
         return formula;
@@ -282,7 +283,7 @@ int resident_clusters(int tile_n, int m_pad, int split_k, int smem, int sms, boo
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)(split_k * 1024), 1, 1);
-    cfg.blockDim = dim3(lowm::kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -391,6 +392,19 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     t->persistent = persistent ? 1 : 0;
     t->tiles_per_cluster = (tiles + clusters - 1) / clusters;
     t->kb_per_stage = kbs;
+    t->mma_issuers = persistent ? 1 : 2;
+    // W stages requested ahead of the programmatic-dependency wait when the
+    // caller promises that the preceding kernel does not write W: the whole
+    // ring, except for rings of three or more 64-column stages (M <= 8 at
+    // N 6144, K 4096), where one stage measured fastest on GB300 (9.95 us
+    // against 10.51 us for the whole ring at M4 N6144 K4096; the whole ring
+    // was fastest for every other shape of the sweep).  LOWM_W_PREFETCH
+    // overrides (tuning).
+    int wpf = (!persistent && tile_n == 64 && stages >= 3) ? 1 : stages;
+    const int force_wpf = env_int("LOWM_W_PREFETCH", -1);
+    if (force_wpf >= 0)
+        wpf = std::min(force_wpf, stages);
+    t->w_prefetch_stages = wpf;
     return LOWM_OK;
 }
 
@@ -514,7 +528,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     p.num_tiles = t.tiles;
     p.timeout_ns = lowm::kDefaultTimeoutNs;
     p.reduce_timeout_ns = lowm::kDefaultTimeoutNs;
-    p.w_before_pdl_wait = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) ? 1u : 0u;
+    p.w_prefetch_stages = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) ? (uint32_t)t.w_prefetch_stages : 0u;
     if (dbg) {
         p.stall_warp_mask = dbg->stall_warp_mask;
         p.stall_rank_mask = dbg->stall_rank_mask;
@@ -530,7 +544,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)t.ctas, 1, 1);
-    cfg.blockDim = dim3(lowm::kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)(t.persistent ? lowm::kThreadsPersistent : lowm::kThreads), 1, 1);
     cfg.dynamicSmemBytes = (size_t)t.smem_bytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attrs[3];

@@ -12,12 +12,19 @@
 //               size, so fewer, larger copies are what lets one CTA stream
 //               its share of HBM bandwidth.
 //   warp 1      MMA warp: allocates TMEM, issues tcgen05.mma (swap-AB: the W
-//               tile is the MMA's A operand with M = 64, the activation tile
-//               is its B operand with N = m_pad), releases each stage with
+//               tile is the MMA's A operand with M = tile_n, the activation
+//               tile is its B operand with N = m_pad) for the even K16 steps
+//               of every stage into accumulator 0, releases each stage with
 //               tcgen05.commit, and frees TMEM after the epilogue's loads.
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, split-K
-//               exchange through the owner's shared-memory mailbox, fp32 ->
-//               bf16 and 16-byte stores of C.
+//   warp 6      second MMA issuer: the odd K16 steps of every stage into
+//               accumulator 1.  One thread issues a tcgen05.mma only every
+//               ~55 cycles whatever the shape (measured on GB300), which at
+//               m_pad 8 makes a single issuer the pace-setter of a CTA's
+//               stream; two issuers halve the time a stage is held.
+//   warps 2..5  epilogue: tcgen05.ld of both fp32 accumulators, summed
+//               (accumulator 0 + accumulator 1), split-K exchange through the
+//               owner's shared-memory mailbox, fp32 -> bf16 and 16-byte
+//               stores of C.
 //
 // Sources for the method ("Fix two synchronization gaps in the MiniMax M3
 // low-M split-K GEMM", TensorRT-LLM PR):
@@ -49,8 +56,11 @@ namespace lowm {
 constexpr int kBlockK = 64;         // K elements per block (one 128-byte swizzle row of bf16)
 constexpr int kMmaK = 16;           // K per tcgen05.mma of kind::f16
 constexpr int kMaxKbPerStage = 8;   // K blocks per stage: 1, 2, 4 or 8
-constexpr int kThreads = 192;       // 6 warps
+constexpr int kThreads = 224;       // lowm_splitk_kernel: 7 warps (TMA, MMA, 4 epilogue, second MMA issuer)
+constexpr int kThreadsPersistent = 192;   // lowm_splitk_persistent_kernel: 6 warps, one MMA issuer
 constexpr int kEpilogueWarp0 = 2;   // warps 2..5; warp % 4 covers every TMEM lane quarter once
+constexpr int kMmaWarp2 = 6;        // second MMA issuer of lowm_splitk_kernel
+constexpr uint32_t kMmaHandoffBarrier = 2;   // named barrier: MMA warp -> second issuer (TMEM address)
 constexpr int kEpilogueThreads = 128;
 __host__ __device__ constexpr uint32_t w_block_bytes(int tile_n)   // one tile_n x 64 W block
 {
@@ -86,7 +96,8 @@ struct KernelParams {
     // test hooks
     uint32_t stall_warp_mask, stall_rank_mask, stall_ns;
     uint32_t drop_mailbox;  // non-owner ranks skip their publication (the owner's wait runs out)
-    uint32_t w_before_pdl_wait;   // caller's promise: the preceding kernel does not write W
+    uint32_t w_prefetch_stages;   // stages of W requested before the programmatic-dependency wait
+                                  // (0 unless the caller promised the preceding kernel does not write W)
     unsigned long long *probes;
     float *c_f32;
     unsigned long long *timeline;   // [4 * ctas]: prologue end, first / last full stage, epilogue end
@@ -185,19 +196,23 @@ __device__ __forceinline__ void load_accumulator(uint32_t taddr, float (&acc)[M_
     ptx::tmem_wait_ld();
 }
 
-// One stage's MMAs: kb_per_stage blocks x 4 K16 steps into the accumulator at
-// tmem_d.  `first` clears the accumulator with the stage's first MMA.
-template <int TILE_N, int M_PAD>
+// One issuer's share of a stage's MMAs into the accumulator at tmem_d: of
+// every block's 4 K16 steps, issuer q of ISSUERS takes kk = q, q + ISSUERS, ...
+// `first` clears the accumulator with this issuer's first MMA of the stage.
+template <int TILE_N, int M_PAD, int ISSUERS>
 __device__ __forceinline__ void mma_stage(uint32_t tmem_d, uint32_t w_stage, uint32_t a_stage, int kb_per_stage,
-                                          bool first)
+                                          bool first, int q)
 {
     constexpr uint32_t kIdesc = make_idesc_bf16(TILE_N, M_PAD);
+    static_assert((kBlockK / kMmaK) % ISSUERS == 0, "issuers split the K16 steps of a block evenly");
     for (int j = 0; j < kb_per_stage; ++j) {
         const uint64_t adesc = make_sw128_kmajor_desc(w_stage + (uint32_t)j * w_block_bytes(TILE_N));
         const uint64_t bdesc = make_sw128_kmajor_desc(a_stage + (uint32_t)j * (M_PAD * 128u));
 #pragma unroll
-        for (int kk = 0; kk < kBlockK / kMmaK; ++kk)      // +32 bytes of K per step: +2 in the encoded address
-            ptx::mma_bf16_ss(tmem_d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (first && j == 0 && kk == 0) ? 0u : 1u);
+        for (int i = 0; i < kBlockK / kMmaK / ISSUERS; ++i) {
+            const uint32_t kk = (uint32_t)(i * ISSUERS + q);    // +32 bytes of K per step: +2 in the encoded address
+            ptx::mma_bf16_ss(tmem_d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (first && j == 0 && i == 0) ? 0u : 1u);
+        }
     }
 }
 
@@ -234,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   "m_pad is the MMA N: a multiple of 8 (M = 64) or 16 (M = 128), at most 64");
     constexpr int kTileN = TILE_N;
     static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
-    constexpr uint32_t kTmemCols = tmem_cols_for(M_PAD);
+    constexpr uint32_t kAcc1 = M_PAD <= 16 ? 16u : (uint32_t)M_PAD;   // column of accumulator 1
+    constexpr uint32_t kTmemCols = tmem_cols_for(kAcc1 + M_PAD);
     constexpr uint32_t kSlotBytes = kTileN * M_PAD * 4u;          // one rank's fp32 partial tile
 
     extern __shared__ uint8_t smem_raw[];
@@ -264,9 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(bar_full + 8u * s, 1);
-            ptx::mbar_init(bar_empty + 8u * s, 1);
+            ptx::mbar_init(bar_empty + 8u * s, 2);        // one tcgen05.commit from each MMA issuer
         }
-        ptx::mbar_init(bar_acc, 1);
+        ptx::mbar_init(bar_acc, 2);                        // each issuer's final commit
         ptx::mbar_init(bar_tmem_alloc, kTmemBarArrivals);
         ptx::mbar_init(bar_reduce, 1);
         if (SPLIT_K > 1 && rank == 0)     // arm the mailbox: every peer sends one full partial tile
@@ -293,10 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = ptx::policy_evict_first();   // W is streamed once
             const uint64_t pol_a = ptx::policy_evict_last();    // A is re-read by every CTA
             // With the caller's promise that W is not written by the preceding
-            // kernel, the first ring of W is requested before the
-            // programmatic-dependency wait, overlapping that kernel's tail.  A
-            // (and C, in the epilogue) are touched only after the wait.
-            const int pre = p.w_before_pdl_wait ? (n_stages < stages ? n_stages : stages) : 0;
+            // kernel, the first w_prefetch_stages stages of W are requested
+            // before the programmatic-dependency wait, overlapping that
+            // kernel's tail.  A (and C, in the epilogue) are touched only after
+            // the wait.
+            int pre = n_stages < stages ? n_stages : stages;
+            if (pre > (int)p.w_prefetch_stages)
+                pre = (int)p.w_prefetch_stages;
             for (int i = 0; i < pre; ++i) {            // fresh ring: these stages are free
                 ptx::mbar_arrive_expect_tx(bar_full + 8u * i, stage_tx);
                 ptx::tma_load_3d(sbase + L.w + (uint32_t)i * w_stage_bytes, &tmap_w, 0, n0, kb0 + i * kbs,
@@ -337,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(tmem_slot, kTmemCols);
         ptx::tmem_relinquish_alloc_permit();       // let other CTAs on this SM allocate early
         ptx::tcgen05_fence_before_thread_sync();
-        __syncwarp();
+        ptx::named_barrier_sync(kMmaHandoffBarrier, 64);   // the second issuer may now read the address
         ptx::tcgen05_fence_after_thread_sync();
         const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot);
         ptx::mbar_arrive(bar_tmem_alloc);          // phase 0: "TMEM allocated" (32 lanes)
@@ -353,11 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.timeline != nullptr && (i == 0 || i == n_stages - 1))
                     p.timeline[4 * blockIdx.x + (i == 0 ? 1 : 2)] = ptx::globaltimer();
                 ptx::tcgen05_fence_after_thread_sync();
-                mma_stage<TILE_N, M_PAD>(tmem_d, sbase + L.w + (uint32_t)s * w_stage_bytes,
-                                 sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, i == 0);
-                ptx::tcgen05_commit(bar_empty + 8u * s);           // stage free once these MMAs have read it
+                mma_stage<TILE_N, M_PAD, 2>(tmem_d, sbase + L.w + (uint32_t)s * w_stage_bytes,
+                                            sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, i == 0, 0);
+                ptx::tcgen05_commit(bar_empty + 8u * s);           // stage free once both issuers' MMAs have read it
             }
-            ptx::tcgen05_commit(bar_acc);                          // accumulator complete
+            ptx::tcgen05_commit(bar_acc);                          // accumulator 0 complete
         }
         __syncwarp();
 
@@ -376,8 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar_tmem_alloc);          // phase 1 (32 lanes)
         if (!wait_bounded<false>(bar_tmem_alloc, 1, p.timeout_ns))
             record_error(p, kErrMmaTmemPhase1);
-        // Every MMA this CTA issued has completed before its columns are freed
-        // (already implied on the normal path, where the epilogue waited for it).
+        // Every MMA this CTA issued (both issuers) has completed before its
+        // columns are freed (already implied on the normal path, where the
+        // epilogue waited for it).
         if (!wait_bounded<false>(bar_acc, 0, kDrainTimeoutNs))
             record_error(p, kErrMmaAccDrain);
         ptx::tcgen05_fence_after_thread_sync();
@@ -388,6 +408,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         ptx::tmem_dealloc(tmem_d, kTmemCols);
+    } else if (warp == kMmaWarp2) {
+        // ------------------------------------------------------------ second MMA issuer
+        // It touches TMEM only after the MMA warp has allocated it (the named
+        // barrier), and the columns are freed only after its final commit has
+        // arrived on bar_acc (the MMA warp's drain wait and the epilogue's
+        // wait both need both commits).
+        ptx::named_barrier_sync(kMmaHandoffBarrier, 64);
+        ptx::tcgen05_fence_after_thread_sync();
+        const uint32_t tmem_d1 = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot) + kAcc1;
+        if (lane == 0) {
+            for (int i = 0; i < n_stages; ++i) {
+                const int s = i % stages;
+                const uint32_t ph = (uint32_t)(i / stages) & 1u;
+                if (!wait_bounded<false>(bar_full + 8u * s, ph, p.timeout_ns)) {
+                    record_error(p, kErrMmaFull);
+                    break;
+                }
+                ptx::tcgen05_fence_after_thread_sync();
+                mma_stage<TILE_N, M_PAD, 2>(tmem_d1, sbase + L.w + (uint32_t)s * w_stage_bytes,
+                                            sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, i == 0, 1);
+                ptx::tcgen05_commit(bar_empty + 8u * s);
+            }
+            ptx::tcgen05_commit(bar_acc);                          // accumulator 1 complete
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue warps
         const int quarter = warp & 3;             // the TMEM lane quarter this warp may access
@@ -413,7 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float acc[M_PAD];
         if (ok) {
-            load_accumulator<M_PAD>(tmem_base + ((uint32_t)(32 * quarter) << 16), acc);
+            const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+            float acc1[M_PAD];
+            load_accumulator<M_PAD>(tmem_base + lanes, acc);
+            load_accumulator<M_PAD>(tmem_base + lanes + kAcc1, acc1);
+#pragma unroll
+            for (int i = 0; i < M_PAD; ++i)
+                acc[i] += acc1[i];                 // fixed order: accumulator 0 + accumulator 1
         } else {
 #pragma unroll
             for (int i = 0; i < M_PAD; ++i)

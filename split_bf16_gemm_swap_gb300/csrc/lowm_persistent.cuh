@@ -28,7 +28,7 @@
 namespace lowm {
 
 template <int TILE_N, int M_PAD, int SPLIT_K>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsPersistent, 1)
     lowm_splitk_persistent_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                   const __grid_constant__ CUtensorMap tmap_w, const KernelParams p)
 {
@@ -108,7 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = ptx::policy_evict_first();
             const uint64_t pol_a = ptx::policy_evict_last();
             const int total = my_tiles * spt;      // (tile, stage) pairs, tile-major
-            const int pre = p.w_before_pdl_wait ? (total < stages ? total : stages) : 0;
+            int pre = total < stages ? total : stages;
+            if (pre > (int)p.w_prefetch_stages)
+                pre = (int)p.w_prefetch_stages;
             for (int i = 0; i < pre; ++i) {
                 const int n0 = (cluster + (i / spt) * clusters) * kTileN;
                 ptx::mbar_arrive_expect_tx(bar_full + 8u * i, stage_tx);
@@ -178,8 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.timeline != nullptr && (i == 0 || i == my_tiles * spt - 1))
                         p.timeline[4 * blockIdx.x + (i == 0 ? 1 : 2)] = ptx::globaltimer();
                     ptx::tcgen05_fence_after_thread_sync();
-                    mma_stage<TILE_N, M_PAD>(d, sbase + L.w + (uint32_t)s * w_stage_bytes,
-                                     sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, st == 0);
+                    mma_stage<TILE_N, M_PAD, 1>(d, sbase + L.w + (uint32_t)s * w_stage_bytes,
+                                                sbase + L.a + (uint32_t)s * a_stage_bytes, kbs, st == 0, 0);
                     ptx::tcgen05_commit(bar_empty + 8u * s);
                 }
                 ptx::tcgen05_commit(bar_acc_full + 8u * b);

@@ -141,6 +141,33 @@ def test_any_n_is_tiled_with_a_partial_last_tile(L, M, N, K, sk):
         assert tn == 64          # 128-column tiles only where they divide N (unless forced)
 
 
+@pytest.mark.parametrize("M,N,K,sk,wpf", [
+    # one W stage ahead of the PDL wait for three-stage 64-column rings, the whole ring otherwise (GB300 sweep)
+    (4, 6144, 4096, 2, 1), (1, 6144, 4096, 2, 1), (8, 6144, 4096, 2, 1), (4, 2304, 12288, 4, 2), (4, 49152, 4096, 2, 2),
+    (16, 6144, 32768, 4, 2), (64, 6144, 4096, 2, 3), (32, 6144, 4096, 2, 2)])
+def test_two_mma_issuers_and_prefetch_depth(L, M, N, K, sk, wpf):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    assert st == lowm.LOWM_OK and t["mma_issuers"] == 2 and t["persistent"] == 0
+    assert t["w_prefetch_stages"] == wpf <= t["stages"]
+
+
+def test_prefetch_depth_override_is_capped_by_the_ring(L, monkeypatch):
+    monkeypatch.setenv("LOWM_W_PREFETCH", "9")
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and t["w_prefetch_stages"] == t["stages"]
+    monkeypatch.setenv("LOWM_W_PREFETCH", "0")
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and t["w_prefetch_stages"] == 0
+
+
+def test_persistent_schedule_has_one_issuer(L, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")
+    st, t = lowm.lowm_gemm_query_tactic(4, 49152, 4096, 2)
+    assert st == lowm.LOWM_OK
+    if t["persistent"]:
+        assert t["mma_issuers"] == 1
+
+
 def test_auto_split_k_keeps_the_k_loop_non_empty(L):
     for M, N, K in [(4, 64, 64), (4, 64, 128), (4, 6144, 4096), (64, 64, 512), (1, 49152, 4096)]:
         st, t = lowm.lowm_gemm_query_tactic(M, N, K, 0)
