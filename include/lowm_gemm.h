@@ -5,7 +5,7 @@
  *
  *     C[M,N] = A[M,K] . W[N,K]^T        bf16 inputs, fp32 accumulation, bf16 output
  *
- * for small M (1..64): a weight matrix W is streamed once from HBM while the
+ * for small M (1..128): a weight matrix W is streamed once from HBM while the
  * few activation rows A are reused by every CTA.  This is the operation of the
  * low-M split-K GEMM described in the TensorRT-LLM PR "Fix two synchronization
  * gaps in the MiniMax M3 low-M split-K GEMM" (Description; Hardware
@@ -59,7 +59,7 @@ typedef enum {
  * A tactic: how one GEMM is tiled and launched.
  *   tile_n       output columns per CTA; the MMA's M dimension (swap-AB: N is
  *                mapped onto the tensor core's M, the tiny M onto its N)
- *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32 or 64);
+ *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64 or 128);
  *                rows M..m_pad-1 are zero-filled by the TMA unit and never stored
  *   split_k      CTAs per cluster along K (1, 2, 4 or 8)
  *   stages       depth of the shared-memory ring between the TMA producer and the MMA warp
@@ -101,7 +101,8 @@ typedef struct {
 
 /*
  * C = A . W^T on `stream`.
- *   M        1..64
+ *   M        1..128 (M > 64 pads to m_pad 128; those shapes run split_k 1, 2
+ *            or 4 with 64-column tiles, 1 or 2 with 128-column tiles)
  *   N        any positive value; when N is not a multiple of tile_n the last
  *            tile is partial (the TMA unit zero-fills W rows >= N and the
  *            epilogue stores only columns < N; 16-byte stores when N % 8 == 0,

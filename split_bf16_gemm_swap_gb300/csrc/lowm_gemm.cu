@@ -126,7 +126,7 @@ int env_int(const char *name, int dflt)
 
 int m_pad_of(int M)
 {
-    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
 }
 
 int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs)
@@ -188,19 +188,22 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, 
 
 bool shape_ok(int M, int N, int K, int split_k)
 {
-    return M >= 1 && M <= 64 && N > 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
+    return M >= 1 && M <= 128 && N > 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
 }
 
 // split_k = 0: the smallest split (1, 2, 4, 8) that keeps the K loop non-empty
 // and gives at least one CTA per SM (counted in 64-column tiles), preferring
-// fewer cluster reductions.
+// fewer cluster reductions; never a split whose mailbox leaves no room for a
+// two-stage ring (m_pad 128 stops at split_k 4).
 int choose_split_k(int M, int N, int K, int sms)
 {
-    (void)M;
     const int tiles = (N + 63) / 64;
+    const int mp = m_pad_of(M);
     int best = 0;
     for (int sk = 1; sk <= 8; sk *= 2) {
         if (K % (sk * lowm::kBlockK) != 0)
+            break;
+        if (footprint(64, mp, sk, 2, 1, 1) > kMaxSmemPerCta || (mp == 128 && sk > 4))
             break;
         best = sk;
         if (tiles * sk >= sms)
@@ -212,6 +215,8 @@ int choose_split_k(int M, int N, int K, int sms)
 // ------------------------------------------------------------------ kernels
 KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent)
 {
+    if (m_pad == 128)
+        return persistent ? nullptr : lowm::kernel_mpad128(tile_n, sk);
     if (tile_n == 64)
         return lowm::kernel_tile64(m_pad, sk, persistent);
     if (tile_n == 128)
@@ -336,7 +341,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     if (tile_n == 128 && m_pad < 16)
         m_pad = 16;                                     // MMA M = 128 needs N a multiple of 16
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1).
-    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1;
+    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad != 128;   // no persistent m_pad 128 instance
     int tiles = (N + tile_n - 1) / tile_n;            // the last tile may be partial
     int clusters = tiles;
     Ring ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
@@ -354,7 +359,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
             ring.stages = stages_override;
         fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1);
     }
-    if (fp > kMaxSmemPerCta)
+    if (fp > kMaxSmemPerCta || !kernel_for(tile_n, m_pad, split_k, false))
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     int smem = full_smem ? kMaxSmemPerCta : fp;
     if (persistent) {
@@ -628,7 +633,7 @@ const char *lowm_status_string(lowm_status_t s)
     switch (s) {
     case LOWM_OK: return "ok";
     case LOWM_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=64, N>=1, K%(split_k*64)==0)";
+    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=128, N>=1, K%(split_k*64)==0, and a split-K mailbox that fits)";
     case LOWM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case LOWM_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103 (GB300)";
     case LOWM_ERR_CUDA: return "CUDA runtime error";

@@ -224,9 +224,12 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     };
     if (poll())
         return true;
+    // The clock is read once per 1024 polls: reading it every 32 polls cost
+    // 0.1-0.5 % of a GEMM on GB300 (N6144 / N2304 / N49152 / M64 shapes);
+    // every 1024 the bound stays far below the 2 s limit's resolution needs.
     const uint64_t t0 = ptx::globaltimer();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 1024; ++i)
             if (poll())
                 return true;
         if (ptx::globaltimer() - t0 > timeout_ns)
@@ -239,14 +242,38 @@ __device__ __forceinline__ void record_error(const KernelParams &p, uint32_t bit
     atomicOr(p.status, bits);
 }
 
+// The owner's stores of one staged tile: rows m < M of [m_pad][tile_n] bf16
+// staging, columns below N.  16-byte stores when N % 8 == 0 (row m of the tile
+// is tile_n / 8 chunks; a partial last tile stores only the chunks below N),
+// element stores otherwise (rows of C are then not 16-byte aligned).
+template <int TILE_N>
+__device__ __forceinline__ void store_tile(const KernelParams &p, const __nv_bfloat16 *stage_out, int n0, int etid)
+{
+    if ((p.N & 7) == 0) {
+        for (int c = etid; c < p.M * (TILE_N / 8); c += kEpilogueThreads) {
+            const int m = c / (TILE_N / 8), ch = c % (TILE_N / 8);   // 16-byte chunk ch of row m
+            if (n0 + ch * 8 < p.N) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * TILE_N + ch * 8);
+                *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
+            }
+        }
+    } else {
+        for (int e = etid; e < p.M * TILE_N; e += kEpilogueThreads) {
+            const int m = e / TILE_N, col = e % TILE_N;
+            if (n0 + col < p.N)
+                p.C[(size_t)m * p.N + n0 + col] = stage_out[m * TILE_N + col];
+        }
+    }
+}
+
 template <int TILE_N, int M_PAD, int SPLIT_K>
 __global__ void __launch_bounds__(kThreads, 1)
     lowm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
                        const KernelParams p)
 {
     static_assert(TILE_N == 64 || TILE_N == 128, "tile_n is the MMA M");
-    static_assert(M_PAD % (TILE_N == 128 ? 16 : 8) == 0 && M_PAD >= 8 && M_PAD <= 64,
-                  "m_pad is the MMA N: a multiple of 8 (M = 64) or 16 (M = 128), at most 64");
+    static_assert(M_PAD % (TILE_N == 128 ? 16 : 8) == 0 && M_PAD >= 8 && M_PAD <= 128,
+                  "m_pad is the MMA N: a multiple of 8 (M = 64) or 16 (M = 128), at most 128");
     constexpr int kTileN = TILE_N;
     static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
     constexpr uint32_t kAcc1 = M_PAD <= 16 ? 16u : (uint32_t)M_PAD;   // column of accumulator 1
@@ -456,101 +483,176 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tcgen05_fence_after_thread_sync();
         ok = __all_sync(0xffffffffu, ok);          // tcgen05.ld is warp-collective
 
-        float acc[M_PAD];
-        if (ok) {
-            const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
-            float acc1[M_PAD];
-            load_accumulator<M_PAD>(tmem_base + lanes, acc);
-            load_accumulator<M_PAD>(tmem_base + lanes + kAcc1, acc1);
+        if constexpr (M_PAD <= 64) {
+            float acc[M_PAD];
+            if (ok) {
+                const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+                float acc1[M_PAD];
+                load_accumulator<M_PAD>(tmem_base + lanes, acc);
+                load_accumulator<M_PAD>(tmem_base + lanes + kAcc1, acc1);
 #pragma unroll
-            for (int i = 0; i < M_PAD; ++i)
-                acc[i] += acc1[i];                 // fixed order: accumulator 0 + accumulator 1
-        } else {
+                for (int i = 0; i < M_PAD; ++i)
+                    acc[i] += acc1[i];                 // fixed order: accumulator 0 + accumulator 1
+            } else {
 #pragma unroll
-            for (int i = 0; i < M_PAD; ++i)
-                acc[i] = 0.0f;
-        }
-        if (p.probes != nullptr) {
-            unsigned long long t = ptx::globaltimer();
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
-            if (lane == 0)
-                atomicMax(&p.probes[2 * blockIdx.x], t);
-        }
-        ptx::tcgen05_fence_before_thread_sync();
-        ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
-
-        int row;
-        const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
-        if (SPLIT_K > 1 && rank != 0) {
-            // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
-            if (ok && valid && !p.drop_mailbox) {
-                const uint32_t dst = ptx::mapa_shared(
-                    sbase + L.mailbox + ((rank - 1u) * kTileN + (uint32_t)row) * (M_PAD * 4u), 0);
-                const uint32_t rbar = ptx::mapa_shared(bar_reduce, 0);
-#pragma unroll
-                for (int i = 0; i < M_PAD / 4; ++i)
-                    ptx::st_async_v4(dst + 16u * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                for (int i = 0; i < M_PAD; ++i)
+                    acc[i] = 0.0f;
             }
-            if (p.timeline != nullptr && etid == 0)
-                p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
+            if (p.probes != nullptr) {
+                unsigned long long t = ptx::globaltimer();
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+                if (lane == 0)
+                    atomicMax(&p.probes[2 * blockIdx.x], t);
+            }
+            ptx::tcgen05_fence_before_thread_sync();
+            ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
+
+            int row;
+            const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
+            if (SPLIT_K > 1 && rank != 0) {
+                // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
+                if (ok && valid && !p.drop_mailbox) {
+                    const uint32_t dst = ptx::mapa_shared(
+                        sbase + L.mailbox + ((rank - 1u) * kTileN + (uint32_t)row) * (M_PAD * 4u), 0);
+                    const uint32_t rbar = ptx::mapa_shared(bar_reduce, 0);
+#pragma unroll
+                    for (int i = 0; i < M_PAD / 4; ++i)
+                        ptx::st_async_v4(dst + 16u * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                }
+                if (p.timeline != nullptr && etid == 0)
+                    p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
+            } else {
+                if (SPLIT_K > 1) {
+                    // Owner: relaxed cluster-scope observation of the mailbox phase,
+                    // then one acquire fence restricted to shared::cluster memory.
+                    if (!wait_bounded<true>(bar_reduce, 0, p.reduce_timeout_ns)) {
+                        record_error(p, kErrReduce);
+                        ok = false;
+                    }
+                    ptx::fence_acquire_shared_cluster();
+                    if (valid && ok) {
+                        const float *box = reinterpret_cast<const float *>(smem + L.mailbox);
+#pragma unroll 1
+                        for (int r = 1; r < SPLIT_K; ++r) {            // fixed rank order
+                            const float4 *src =
+                                reinterpret_cast<const float4 *>(box + ((r - 1) * kTileN + row) * M_PAD);
+#pragma unroll
+                            for (int i = 0; i < M_PAD / 4; ++i) {
+                                const float4 v = src[i];
+                                acc[4 * i] += v.x;
+                                acc[4 * i + 1] += v.y;
+                                acc[4 * i + 2] += v.z;
+                                acc[4 * i + 3] += v.w;
+                            }
+                        }
+                    }
+                }
+                __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
+                if (valid) {
+#pragma unroll
+                    for (int m = 0; m < M_PAD; ++m)
+                        stage_out[m * kTileN + row] = __float2bfloat16_rn(acc[m]);
+                    if (p.c_f32 != nullptr) {
+#pragma unroll
+                        for (int m = 0; m < M_PAD; ++m)
+                            if (m < p.M && n0 + row < p.N)
+                                p.c_f32[(size_t)m * p.N + n0 + row] = acc[m];
+                    }
+                }
+                ptx::named_barrier_sync(1, kEpilogueThreads);
+                store_tile<kTileN>(p, stage_out, n0, etid);
+                if (p.timeline != nullptr && etid == 0)
+                    p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
+            }
         } else {
-            if (SPLIT_K > 1) {
-                // Owner: relaxed cluster-scope observation of the mailbox phase,
-                // then one acquire fence restricted to shared::cluster memory.
+            // m_pad 128: two 128-column accumulators do not fit in registers, so
+            // the epilogue works in 32-column chunks.  The owner waits for the
+            // whole mailbox first; every thread makes its second (TMEM-release)
+            // arrival only after its last chunk's tcgen05.wait::ld.
+            constexpr int kCh = 32;
+            const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+            int row;
+            const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
+            const bool owner = !(SPLIT_K > 1 && rank != 0);
+            if (owner && SPLIT_K > 1) {
                 if (!wait_bounded<true>(bar_reduce, 0, p.reduce_timeout_ns)) {
                     record_error(p, kErrReduce);
                     ok = false;
                 }
                 ptx::fence_acquire_shared_cluster();
-                if (valid && ok) {
-                    const float *box = reinterpret_cast<const float *>(smem + L.mailbox);
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
+            const float *box = reinterpret_cast<const float *>(smem + L.mailbox);
+            uint32_t dst = 0, rbar = 0;
+            if (!owner) {
+                dst = ptx::mapa_shared(sbase + L.mailbox + ((rank - 1u) * kTileN + (uint32_t)row) * (M_PAD * 4u), 0);
+                rbar = ptx::mapa_shared(bar_reduce, 0);
+            }
 #pragma unroll 1
-                    for (int r = 1; r < SPLIT_K; ++r) {            // fixed rank order
-                        const float4 *src =
-                            reinterpret_cast<const float4 *>(box + ((r - 1) * kTileN + row) * M_PAD);
+            for (int c0 = 0; c0 < M_PAD; c0 += kCh) {
+                float acc[kCh];
+                if (ok) {
+                    float acc1[kCh];
+                    load_accumulator<kCh>(tmem_base + lanes + (uint32_t)c0, acc);
+                    load_accumulator<kCh>(tmem_base + lanes + kAcc1 + (uint32_t)c0, acc1);
 #pragma unroll
-                        for (int i = 0; i < M_PAD / 4; ++i) {
-                            const float4 v = src[i];
-                            acc[4 * i] += v.x;
-                            acc[4 * i + 1] += v.y;
-                            acc[4 * i + 2] += v.z;
-                            acc[4 * i + 3] += v.w;
+                    for (int i = 0; i < kCh; ++i)
+                        acc[i] += acc1[i];             // fixed order: accumulator 0 + accumulator 1
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kCh; ++i)
+                        acc[i] = 0.0f;
+                }
+                if (!owner) {
+                    if (ok && valid && !p.drop_mailbox) {
+#pragma unroll
+                        for (int i = 0; i < kCh / 4; ++i)
+                            ptx::st_async_v4(dst + 4u * (uint32_t)c0 + 16u * i, rbar, acc[4 * i], acc[4 * i + 1],
+                                             acc[4 * i + 2], acc[4 * i + 3]);
+                    }
+                } else if (valid) {
+                    if (SPLIT_K > 1 && ok) {
+#pragma unroll 1
+                        for (int r = 1; r < SPLIT_K; ++r) {    // fixed rank order
+                            const float4 *src =
+                                reinterpret_cast<const float4 *>(box + ((r - 1) * kTileN + row) * M_PAD + c0);
+#pragma unroll
+                            for (int i = 0; i < kCh / 4; ++i) {
+                                const float4 v = src[i];
+                                acc[4 * i] += v.x;
+                                acc[4 * i + 1] += v.y;
+                                acc[4 * i + 2] += v.z;
+                                acc[4 * i + 3] += v.w;
+                            }
                         }
                     }
-                }
-            }
-            __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
-            if (valid) {
 #pragma unroll
-                for (int m = 0; m < M_PAD; ++m)
-                    stage_out[m * kTileN + row] = __float2bfloat16_rn(acc[m]);
-                if (p.c_f32 != nullptr) {
+                    for (int i = 0; i < kCh; ++i)
+                        stage_out[(c0 + i) * kTileN + row] = __float2bfloat16_rn(acc[i]);
+                    if (p.c_f32 != nullptr) {
 #pragma unroll
-                    for (int m = 0; m < M_PAD; ++m)
-                        if (m < p.M && n0 + row < p.N)
-                            p.c_f32[(size_t)m * p.N + n0 + row] = acc[m];
-                }
-            }
-            ptx::named_barrier_sync(1, kEpilogueThreads);
-            if ((p.N & 7) == 0) {
-                // 16-byte coalesced stores: row m of the tile is tile_n bf16 = tile_n / 8
-                // chunks; a partial last tile stores only the chunks below N.
-                for (int c = etid; c < p.M * (kTileN / 8); c += kEpilogueThreads) {
-                    const int m = c / (kTileN / 8), ch = c % (kTileN / 8);   // 16-byte chunk ch of row m
-                    if (n0 + ch * 8 < p.N) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * kTileN + ch * 8);
-                        *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
+                        for (int i = 0; i < kCh; ++i)
+                            if (c0 + i < p.M && n0 + row < p.N)
+                                p.c_f32[(size_t)(c0 + i) * p.N + n0 + row] = acc[i];
                     }
                 }
-            } else {
-                // N not a multiple of 8: rows of C are not 16-byte aligned; store elements.
-                for (int e = etid; e < p.M * kTileN; e += kEpilogueThreads) {
-                    const int m = e / kTileN, col = e % kTileN;
-                    if (n0 + col < p.N)
-                        p.C[(size_t)m * p.N + n0 + col] = stage_out[m * kTileN + col];
-                }
+            }
+            if (p.probes != nullptr) {
+                unsigned long long t = ptx::globaltimer();
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+                if (lane == 0)
+                    atomicMax(&p.probes[2 * blockIdx.x], t);
+            }
+            ptx::tcgen05_fence_before_thread_sync();
+            ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
+            if (owner) {
+                ptx::named_barrier_sync(1, kEpilogueThreads);
+                store_tile<kTileN>(p, stage_out, n0, etid);
             }
             if (p.timeline != nullptr && etid == 0)
                 p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();

@@ -16,5 +16,8 @@ typedef void (*KernelFn)(CUtensorMap, CUtensorMap, KernelParams);
 // instance exists.
 KernelFn kernel_tile64(int m_pad, int split_k, bool persistent);
 KernelFn kernel_tile128(int m_pad, int split_k, bool persistent);
+// m_pad 128 (one-tile schedule): tile_n 64 with split_k 1, 2, 4; tile_n 128
+// with split_k 1, 2; nullptr otherwise.
+KernelFn kernel_mpad128(int tile_n, int split_k);
 
 }  // namespace lowm

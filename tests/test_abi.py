@@ -65,7 +65,8 @@ def test_default_tactic_for_the_headline_workload(L):
     assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["persistent"] == 0 and t["smem_bytes"] <= 232448
 
 
-@pytest.mark.parametrize("M,tile", [(4, 64), (8, 64), (9, 128), (16, 128), (17, 64), (32, 64), (33, 128), (64, 128)])
+@pytest.mark.parametrize("M,tile", [(4, 64), (8, 64), (9, 128), (16, 128), (17, 64), (32, 64), (33, 128), (64, 128),
+                                    (65, 64), (128, 64)])
 def test_tile_width_follows_m_pad(L, M, tile):
     st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 2)
     assert st == lowm.LOWM_OK and t["tile_n"] == tile
@@ -168,6 +169,25 @@ def test_persistent_schedule_has_one_issuer(L, monkeypatch):
         assert t["mma_issuers"] == 1
 
 
+@pytest.mark.parametrize("M", [65, 96, 127, 128])
+def test_m_up_to_128_pads_to_128(L, M, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")      # no persistent m_pad 128 instance: ignored
+    for sk in (1, 2, 4):
+        st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, sk)
+        assert st == lowm.LOWM_OK and t["m_pad"] == 128 and t["persistent"] == 0 and t["mma_issuers"] == 2
+        assert t["smem_bytes"] <= 232448
+    st, t = lowm.lowm_gemm_query_tactic(M, 64, 8192, 0)   # one tile: auto split stops where the mailbox fits
+    assert st == lowm.LOWM_OK and t["split_k"] == 4
+
+
+def test_forced_128_column_tiles_at_m_pad_128(L, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", "128")
+    st, t = lowm.lowm_gemm_query_tactic(128, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and t["tile_n"] == 128 and t["m_pad"] == 128
+    st, t = lowm.lowm_gemm_query_tactic(128, 6144, 4096, 4)    # no 128-column split-4 instance: 64 columns
+    assert st == lowm.LOWM_OK and t["tile_n"] == 64
+
+
 def test_auto_split_k_keeps_the_k_loop_non_empty(L):
     for M, N, K in [(4, 64, 64), (4, 64, 128), (4, 6144, 4096), (64, 64, 512), (1, 49152, 4096)]:
         st, t = lowm.lowm_gemm_query_tactic(M, N, K, 0)
@@ -177,7 +197,8 @@ def test_auto_split_k_keeps_the_k_loop_non_empty(L):
 
 @pytest.mark.parametrize("M,N,K,sk,want", [
     (0, 64, 64, 1, lowm.LOWM_ERR_INVALID_ARGUMENT),
-    (65, 64, 64, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),
+    (129, 64, 64, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),
+    (128, 64, 1024, 8, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),   # m_pad 128: the split-8 mailbox does not fit
     (4, 64, 96, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # K not a multiple of 64
     (4, 64, 64, 2, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # empty K loop on one rank
     (4, 64, 128, 3, lowm.LOWM_ERR_INVALID_ARGUMENT),      # split_k not a power of two

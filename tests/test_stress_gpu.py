@@ -72,6 +72,7 @@ CONFIGS = [
     (4, 2304, 12288, 4, "randn"),
     (4, 49152, 4096, 2, "randn"),
     (64, 6144, 4096, 2, "randn"),          # 128-column tiles (MMA M = 128)
+    (128, 6144, 4096, 2, "randn"),         # m_pad 128: chunked epilogue, release after the last chunk
 ]
 
 
