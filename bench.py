@@ -42,6 +42,18 @@ METRIC = "HBM GB/s (% of GB300 peak) and us/GEMM, bf16 M=4 N=6144 K=4096 split-K
 UNIT = "GB/s"
 WORKLOAD = dict(M=4, N=6144, K=4096, split_k=2)
 WIDE = dict(M=4, N=49152, K=4096, split_k=2)
+# name -> (M, N, K, split_k); split_k 0 lets the tactic table choose (the M sweep)
+OTHER_CONFIGS = [
+    ("M4 N2304 K12288 split_k 4", (4, 2304, 12288, 4)),
+    ("M16 N6144 K32768 split_k 4", (16, 6144, 32768, 4)),
+    ("M1 N6144 K4096 auto", (1, 6144, 4096, 0)),
+    ("M2 N6144 K4096 auto", (2, 6144, 4096, 0)),
+    ("M8 N6144 K4096 auto", (8, 6144, 4096, 0)),
+    ("M16 N6144 K4096 auto", (16, 6144, 4096, 0)),
+    ("M32 N6144 K4096 auto", (32, 6144, 4096, 0)),
+    ("M64 N6144 K4096 auto", (64, 6144, 4096, 0)),
+    ("M128 N6144 K4096 auto", (128, 6144, 4096, 0)),
+]
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_NAME = "lowm_splitk_kernel"
 
@@ -333,6 +345,22 @@ def run_ours(args):
         "frac": bytes_per * vsteps / vsecs / 1e9 / peak, "steps": vsteps,
         "entry_point": "lowm_gemm_bf16_ex(flags=%d)" % vw["flags"]}
 
+    # The other configurations of the method's workloads (split-K reduction
+    # width, long K, the M sweep, M above 64), same protocol and launch flags,
+    # shorter runs: reported alongside the headline, not part of `value`.
+    others = {}
+    osteps = max(200, min(args.steps, 5000))
+    for name, (M, N, K, sk) in OTHER_CONFIGS:
+        ow = dict(M=M, N=N, K=K, split_k=sk, flags=w["flags"])
+        _, otactic = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+        steps_o = osteps if N * K <= 64 << 20 else max(200, osteps // 5)
+        osecs, _, _ = time_device(lowm, ow, steps_o, max(args.warmup, 3), device)
+        ob = algo_bytes(M, N, K)
+        others[name] = {"us_per_gemm": osecs / steps_o * 1e6, "gbs": ob * steps_o / osecs / 1e9,
+                        "frac": ob * steps_o / osecs / 1e9 / peak, "steps": steps_o,
+                        "tile_n": otactic["tile_n"], "split_k": otactic["split_k"],
+                        "ring": "%d x %d" % (otactic["kb_per_stage"], otactic["stages"])}
+
     e2e_steps = max(5, min(args.steps, 50))
     esecs, h2d, d2h = time_e2e(lowm, w, e2e_steps, device)
     e2e = {"value": bytes_per * e2e_steps / esecs / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -361,6 +389,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": bytes_per, "traffic": committed_traffic(w, tactic)},
         "wide_n": wide,
         "variants": variants,
+        "other_configs": others,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,

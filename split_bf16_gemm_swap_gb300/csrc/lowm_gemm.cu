@@ -140,7 +140,10 @@ int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs)
 //   - a grid that does not fit on the GPU at once wants several small CTAs per
 //     SM (their prologues and epilogues overlap each other's streams): three
 //     per SM without clusters, five with them;
-//   - rings beyond ~160 KiB per CTA gain nothing.
+//   - rings holding more than ~160 KiB of W per CTA gain nothing (W bytes:
+//     the A tiles in the ring come from L2; at m_pad 128 an A block is twice
+//     a 64-column W block, and counting it would cap that ring at 2 x 2
+//     blocks where 4 x 2 measured 15.8 against 17.1 us at M128 N6144 K4096).
 // Hence: budget shared memory for ceil(ctas / sms) CTAs per SM when that is at
 // most 4 (the whole grid resident at once), else for 3 (split_k 1) or 5; take
 // the most blocks per copy (8, 4, 2, 1, dividing the rank's blocks) whose
@@ -163,7 +166,7 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, 
     if (force_kbs && kb_per_rank % force_kbs != 0)
         force_kbs = 0;                                 // a forced value that does not divide is ignored
     const int force_st = env_int("LOWM_STAGES", 0);
-    auto ring_bytes = [&](int kbs, int st) { return st * kbs * (int)(lowm::w_block_bytes(tile_n) + (uint32_t)m_pad * 128u); };
+    auto ring_bytes = [&](int kbs, int st) { return st * kbs * (int)lowm::w_block_bytes(tile_n); };   // W bytes
     int kbs = 1;
     if (force_kbs) {
         kbs = force_kbs;
@@ -194,11 +197,14 @@ bool shape_ok(int M, int N, int K, int split_k)
 // split_k = 0: the smallest split (1, 2, 4, 8) that keeps the K loop non-empty
 // and gives at least one CTA per SM (counted in 64-column tiles), preferring
 // fewer cluster reductions; never a split whose mailbox leaves no room for a
-// two-stage ring (m_pad 128 stops at split_k 4).
+// two-stage ring (m_pad 128 stops at split_k 4).  At m_pad 128 every split
+// costs a tile_n x 128 fp32 mailbox slot and ring depth, so one CTA on half
+// the SMs is enough (M128 N6144 K4096 on GB300: split_k 1 15.8 us, 2 25.6 us).
 int choose_split_k(int M, int N, int K, int sms)
 {
     const int tiles = (N + 63) / 64;
     const int mp = m_pad_of(M);
+    const int want = mp == 128 ? (sms + 1) / 2 : sms;
     int best = 0;
     for (int sk = 1; sk <= 8; sk *= 2) {
         if (K % (sk * lowm::kBlockK) != 0)
@@ -206,7 +212,7 @@ int choose_split_k(int M, int N, int K, int sms)
         if (footprint(64, mp, sk, 2, 1, 1) > kMaxSmemPerCta || (mp == 128 && sk > 4))
             break;
         best = sk;
-        if (tiles * sk >= sms)
+        if (tiles * sk >= want)
             break;
     }
     return best;

@@ -545,3 +545,35 @@ def test_m128_twenty_launches_are_bitwise_identical():
     assert bool((o == o[0:1]).all())
     C = check(A, W, split_k)                      # the same launch configuration against the oracle
     assert np.array_equal(C, inputs.bits(outs[0].cpu()))
+
+
+# ---------------------------------------------------------------- large grids and the Python convenience wrapper
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 1 << 20, 64, 1), (3, (1 << 19) + 40, 128, 2), (128, 1 << 17, 64, 1)])
+def test_large_grids(M, N, K, split_k):
+    # Tens of thousands of CTAs (16384 clusters at N 2^20), a ragged last tile
+    # and the largest m_pad, each against the oracle element by element.
+    A, W = inputs.make_problem(M, N, K, seed=44)
+    check(A, W, split_k)
+
+
+def test_python_gemm_wrapper_allocates_and_raises():
+    M, N, K = 5, 384, 1024
+    A, W = inputs.make_problem(M, N, K, seed=45)
+    C = lowm.gemm(A.to(DEV), W.to(DEV), split_k=2)
+    sync_ok()
+    assert C.shape == (M, N) and C.dtype == torch.bfloat16
+    Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+    F = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16_debug(A.to(DEV), W.to(DEV), Cd, M, N, K, 2, None, c_f32=F) == lowm.LOWM_OK
+    sync_ok()
+    assert torch.equal(C.view(torch.int16), Cd.view(torch.int16))       # the wrapper runs the same kernel
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S,
+                  f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy()))
+    C2 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.gemm(A.to(DEV), W.to(DEV), C2, split_k=2) is C2
+    sync_ok()
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    with pytest.raises(lowm.LowmError) as e:
+        lowm.gemm(A.to(DEV)[:, :96].contiguous(), W.to(DEV)[:, :96].contiguous(), split_k=1)   # K = 96: not a multiple of 64
+    assert e.value.status == lowm.LOWM_ERR_UNSUPPORTED_SHAPE
