@@ -173,8 +173,10 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
  * on the SM, run a TMEM-allocating kernel on a second stream, and probe
  * %globaltimer at the epilogue's tcgen05.ld and the MMA warp's tcgen05.dealloc.
  *
- *   stall_warp_mask  bit w set: warp w of the CTA (epilogue warps are 2..5)
- *                    sleeps stall_ns before its first TMEM-barrier arrival
+ *   stall_warp_mask  bit w set: warp w of the CTA sleeps stall_ns: epilogue
+ *                    warps (2..5) before their first TMEM-barrier arrival, the
+ *                    second MMA issuer (warp 6, one-tile kernel) before its
+ *                    first MMA
  *   stall_rank_mask  bit r set: only cluster ranks r stall (0 = every rank)
  *   stall_ns         stall length in nanoseconds (bounded busy sleep)
  *   full_smem        0: request the kernel's footprint (the default, which

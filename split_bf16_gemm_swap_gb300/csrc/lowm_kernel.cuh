@@ -444,6 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::named_barrier_sync(kMmaHandoffBarrier, 64);
         ptx::tcgen05_fence_after_thread_sync();
         const uint32_t tmem_d1 = *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot) + kAcc1;
+        if (((p.stall_warp_mask >> warp) & 1u) && (p.stall_rank_mask == 0 || ((p.stall_rank_mask >> rank) & 1u))) {
+            const uint64_t t0 = ptx::globaltimer();     // bounded stall before its first MMA (test hook)
+            while (ptx::globaltimer() - t0 < p.stall_ns)
+                ptx::nanosleep(256);
+        }
         if (lane == 0) {
             for (int i = 0; i < n_stages; ++i) {
                 const int s = i % stages;

@@ -37,7 +37,7 @@ def _lib():
     lowm.lib()
 
 
-def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0):
+def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0, warp_mask=STALL_WARPS):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
     assert st == lowm.LOWM_OK
     ctas = t["ctas"]
@@ -49,7 +49,7 @@ def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0
     for i in range(LAUNCHES):
         for _ in range(3):
             assert lowm.lowm_tmem_hog_launch(s_hog, 4096, hog_cols, 4) == lowm.LOWM_OK
-        st = lowm.lowm_gemm_bf16_debug(Ad, Wd, outs[i], M, N, K, split_k, s_gemm, stall_warp_mask=STALL_WARPS,
+        st = lowm.lowm_gemm_bf16_debug(Ad, Wd, outs[i], M, N, K, split_k, s_gemm, stall_warp_mask=warp_mask,
                                        stall_rank_mask=stall_rank_mask, stall_ns=stall_ns, probes=probes[i])
         assert st == lowm.LOWM_OK
     torch.cuda.synchronize()
@@ -98,6 +98,25 @@ def test_stalled_epilogue_with_tmem_hog(M, N, K, split_k, kind):
         bad = int((o != ref.view(torch.int16)[None]).any(dim=2).any(dim=1).sum())
         assert bad == 0, "stall %d ns: %d of %d launches differ from the unstressed output" % (
             stall_ns, bad, LAUNCHES)
+        check_probes(probes)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (16, 6144, 32768, 4), (128, 1024, 4096, 2)])
+def test_stalled_second_mma_issuer_with_tmem_hog(M, N, K, split_k):
+    # The columns may be freed only after both issuers' final commits: delay
+    # the second issuer (warp 6) before its first MMA, with the TMEM hog on a
+    # second stream; outputs must stay bitwise identical and every CTA's
+    # dealloc must follow its epilogue's last load.
+    A, W = inputs.make_problem(M, N, K, seed=1234, kind="int")
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16(Ad, Wd, ref, M, N, K, split_k, None) == lowm.LOWM_OK
+    torch.cuda.synchronize()
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(inputs.bits(ref.cpu()), np.broadcast_to(inputs.bits(col[None, :]), (M, N)))
+    for stall_ns in (5_000, 100_000):
+        outs, probes = stressed(Ad, Wd, M, N, K, split_k, stall_ns, warp_mask=1 << 6)
+        assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
         check_probes(probes)
 
 
