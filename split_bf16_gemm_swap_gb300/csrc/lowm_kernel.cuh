@@ -1,6 +1,6 @@
 // The low-M split-K bf16 GEMM kernel for sm_103a:  C[M,N] = A[M,K] . W[N,K]^T.
 //
-// One CTA owns a 64-column slice of C (tile_n = 64) and 1/split_k of K.  The
+// One CTA owns a tile_n-column slice of C (tile_n = 64 or 128) and 1/split_k of K.  The
 // split_k CTAs of a slice form one thread-block cluster along grid x; rank 0
 // of the cluster is the owner that reduces and stores.  Warp roles:
 //   warp 0      TMA producer: streams W and A through a ring of `stages`
@@ -30,7 +30,9 @@
 // low-M split-K GEMM", TensorRT-LLM PR):
 //   - Description, item 1: the TMEM barrier bar_tmem_alloc with 160 arrivals
 //     (32 MMA-warp lanes + 128 epilogue threads) and two phases; the fix makes
-//     the MMA warp observe phase 0 before its release arrival.
+//     the MMA warp observe phase 0 before its release arrival.  (The second
+//     MMA issuer does not arrive on it: it is ordered by the named-barrier
+//     hand-off before its MMAs and by bar_acc before the dealloc.)
 //   - Description, item 2: peers publish fp32 partials with
 //     st.async ... complete_tx into rank 0's shared memory, crediting
 //     bar_reduce; rank 0 waits with a relaxed cluster-scope parity wait and
@@ -90,7 +92,7 @@ struct KernelParams {
     int stages;             // ring depth
     int kb_per_stage;       // 64-wide K blocks per stage (divides kb_per_rank)
     int kb_per_rank;        // 64-wide K blocks per cluster rank
-    int num_tiles;          // N / 64 (the persistent kernel walks them; the other kernel has one per cluster)
+    int num_tiles;          // ceil(N / tile_n) (the persistent kernel walks them; the other kernel has one per cluster)
     uint64_t timeout_ns;    // bound on every wait for another party
     uint64_t reduce_timeout_ns;   // bound on the owner's mailbox wait
     // test hooks
