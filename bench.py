@@ -359,7 +359,8 @@ def run_ours(args):
         others[name] = {"us_per_gemm": osecs / steps_o * 1e6, "gbs": ob * steps_o / osecs / 1e9,
                         "frac": ob * steps_o / osecs / 1e9 / peak, "steps": steps_o,
                         "tile_n": otactic["tile_n"], "split_k": otactic["split_k"],
-                        "ring": "%d x %d" % (otactic["kb_per_stage"], otactic["stages"])}
+                        "ring": "%d x %d" % (otactic["kb_per_stage"], otactic["stages"]),
+                        "traffic": committed_traffic(dict(M=M, N=N, K=K, split_k=otactic["split_k"]), otactic)}
 
     e2e_steps = max(5, min(args.steps, 50))
     esecs, h2d, d2h = time_e2e(lowm, w, e2e_steps, device)
@@ -476,6 +477,9 @@ def run_profile_case(args):
     __graft_entry__.build()
     from split_bf16_gemm_swap_gb300 import inputs, lowm
     w = dict(WIDE if args.wide else WORKLOAD)
+    if args.config:
+        M, N, K, sk = dict(OTHER_CONFIGS)[args.config]
+        w = dict(M=M, N=N, K=K, split_k=sk)
     M, N, K, sk = w["M"], w["N"], w["K"], w["split_k"]
     device = torch.device("cuda", 0)
     A, W = inputs.make_problem(M, N, K, seed=1234)
@@ -507,6 +511,8 @@ def main():
     ap.add_argument("--profile-only", action="store_true",
                     help="plain launches of the workload for a profiler (no timing, no JSON line)")
     ap.add_argument("--wide", action="store_true", help="with --profile-only: the wide-N workload")
+    ap.add_argument("--config", default=None, choices=[name for name, _ in OTHER_CONFIGS],
+                    help="with --profile-only: one of the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
