@@ -577,3 +577,43 @@ def test_python_gemm_wrapper_allocates_and_raises():
     with pytest.raises(lowm.LowmError) as e:
         lowm.gemm(A.to(DEV)[:, :96].contiguous(), W.to(DEV)[:, :96].contiguous(), split_k=1)   # K = 96: not a multiple of 64
     assert e.value.status == lowm.LOWM_ERR_UNSUPPORTED_SHAPE
+
+
+# ---------------------------------------------------------------- seeded fuzz over shapes and tactic overrides
+def _fuzz_cases(n=60, seed=20261202):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        M = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65, 100, 127, 128]))
+        sk = int(rng.choice([1, 2, 4, 8]))
+        K = 64 * sk * int(rng.integers(1, 9))
+        N = int(rng.choice([int(rng.integers(1, 700)), 64 * int(rng.integers(1, 12))]))
+        env = {"LOWM_TILE_N": str(int(rng.choice([0, 64, 128]))),
+               "LOWM_KB_PER_STAGE": str(int(rng.choice([0, 1, 2, 4, 8]))),
+               "LOWM_STAGES": str(int(rng.choice([0, 2, 3, 4, 6]))),
+               "LOWM_W_PREFETCH": str(int(rng.choice([-1, 0, 1, 2])))}
+        flags = int(rng.integers(0, 2))
+        cases.append((M, N, K, sk, env, flags))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_fuzz_shapes_and_tactics(case, monkeypatch):
+    M, N, K, sk, env, flags = _fuzz_cases()[case]
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    if st == lowm.LOWM_ERR_UNSUPPORTED_SHAPE:
+        # only shapes whose mailbox or forced ring cannot fit may be refused
+        assert (M > 64 and sk == 8) or env["LOWM_STAGES"] != "0" or env["LOWM_KB_PER_STAGE"] != "0"
+        pytest.skip("refused by the host before any launch: %s" % lowm.status_string(st))
+    assert st == lowm.LOWM_OK
+    A, W = inputs.make_problem(M, N, K, seed=900 + case)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    F = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    assert lowm.lowm_gemm_bf16_debug(Ad, Wd, C, M, N, K, sk, None, c_f32=F, flags=flags) == lowm.LOWM_OK
+    sync_ok()
+    Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S,
+                  f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy()))
