@@ -100,7 +100,9 @@ typedef struct {
 } lowm_tactic_t;
 
 /*
- * C = A . W^T on `stream`.
+ * C = A . W^T on `stream`: the low-M split-K GEMM of the PR page
+ * (Description; the launch shape of Hardware verification: clusters of
+ * split_k CTAs along the output columns, programmatic dependent launch on).
  *   M        1..128 (M > 64 pads to m_pad 128; those shapes run split_k 1, 2
  *            or 4 with 64-column tiles, 1 or 2 with 128-column tiles)
  *   N        any positive value; when N is not a multiple of tile_n the last
@@ -110,7 +112,13 @@ typedef struct {
  *   K        a positive multiple of split_k * 64
  *   split_k  0 (let the tactic table choose), 1, 2, 4 or 8
  *   A, W, C  device pointers, 16-byte aligned; C must not overlap A or W
- * Returns LOWM_OK once the kernel is enqueued.
+ * Returns LOWM_OK once the kernel is enqueued.  Errors, all before anything
+ * is enqueued: LOWM_ERR_INVALID_ARGUMENT (a NULL pointer, M, N or K <= 0,
+ * split_k outside {0, 1, 2, 4, 8}, C overlapping A or W),
+ * LOWM_ERR_MISALIGNED, LOWM_ERR_UNSUPPORTED_SHAPE (a rule above, or no
+ * tactic whose shared memory fits), LOWM_ERR_UNSUPPORTED_ARCH; a failed
+ * launch returns LOWM_ERR_CUDA.  The result is deterministic: the same
+ * arguments and tactic give the same bits on every launch.
  */
 lowm_status_t lowm_gemm_bf16(const void *A, const void *W, void *C,
                              int M, int N, int K, int split_k, void *stream);
