@@ -2,7 +2,7 @@
 // table, TMA descriptor encoding (cached), and the cluster + PDL launch.
 //
 // Launch shape ("Fix two synchronization gaps in the MiniMax M3 low-M split-K
-// GEMM", TensorRT-LLM PR, Hardware verification): ceil(N / 64) clusters of split_k
+// GEMM", TensorRT-LLM PR, Hardware verification): ceil(N / tile_n) clusters of split_k
 // CTAs, programmatic dependent launch on, cluster dimension split_k along grid
 // x.  The host also guarantees the non-empty K loop that the PR's analysis of
 // the TMEM race relies on (Description, item 1): K must be a positive
