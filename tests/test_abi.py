@@ -230,3 +230,46 @@ def test_library_does_not_reference_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle." not in text, f
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "lowm_gemm.h"
+
+int main(void)
+{
+    lowm_tactic_t t;
+    lowm_status_t st = lowm_gemm_query_tactic(4, 6144, 4096, 2, &t);
+    if (st != LOWM_OK) { printf("query failed: %s\n", lowm_status_string(st)); return 1; }
+    printf("%d %d %d %d %d %d %d %d\n", t.tile_n, t.m_pad, t.split_k, t.kb_per_stage, t.stages, t.ctas,
+           t.mma_issuers, t.w_prefetch_stages);
+    if (lowm_gemm_query_tactic(129, 64, 64, 1, &t) != LOWM_ERR_UNSUPPORTED_SHAPE) return 2;
+    if (lowm_gemm_bf16(0, 0, 0, 4, 64, 64, 1, 0) != LOWM_ERR_INVALID_ARGUMENT) return 3;
+    if (lowm_gemm_bf16_ex((void *)0x1000, (void *)0x2000, (void *)0x3000, 4, 64, 64, 1, 2u, 0)
+        != LOWM_ERR_INVALID_ARGUMENT) return 4;      /* unknown flag bit */
+    return 0;
+}
+"""
+
+
+def test_the_header_is_c99_and_links_against_the_library(L, tmp_path):
+    # The boundary from plain C: the header compiles as C99, the program links
+    # against liblowm_gemm.so and the host-only entry points answer as the
+    # Python binding does.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(lowm.LIB_PATH)
+    subprocess.check_call([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-L", libdir, "-llowm_gemm", "-Wl,-rpath," + libdir, "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stdout + out.stderr
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    want = [t[k] for k in ("tile_n", "m_pad", "split_k", "kb_per_stage", "stages", "ctas", "mma_issuers",
+                           "w_prefetch_stages")]
+    assert [int(x) for x in out.stdout.split()] == want
