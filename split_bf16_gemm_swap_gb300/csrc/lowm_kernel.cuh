@@ -122,7 +122,7 @@ __host__ __device__ inline SmemLayout make_smem_layout(int tile_n, int m_pad, in
     off += (uint32_t)stages * (uint32_t)kb_per_stage * w_block_bytes(tile_n);
     L.a = off;                                            // [stages][kb_per_stage][m_pad][64 k]; m_pad*128 % 1024 == 0
     off += (uint32_t)stages * (uint32_t)kb_per_stage * (uint32_t)m_pad * 128u;
-    L.mailbox = off;                                      // [bufs][(split_k-1)][tile_n][m_pad] fp32
+    L.mailbox = off;                                      // [bufs][split_k-1] slots of tile_n x m_pad fp32 (*)
     off += (uint32_t)bufs * (uint32_t)(split_k - 1) * (uint32_t)tile_n * (uint32_t)m_pad * 4u;
     L.out = off;                                          // [bufs][m_pad][tile_n] bf16 staging for C
     off += (uint32_t)bufs * (uint32_t)m_pad * (uint32_t)tile_n * 2u;
@@ -133,6 +133,14 @@ __host__ __device__ inline SmemLayout make_smem_layout(int tile_n, int m_pad, in
     L.bytes = off + 1024;                                 // slack to align the dynamic base
     return L;
 }
+// (*) Slot layout.  lowm_splitk_kernel stores a slot as [m_pad / 4][tile_n]
+// float4, so that for one float4 index the rows of a warp are consecutive 16
+// bytes: the peers' st.async writes and the owner's reads are free of bank
+// conflicts.  (Rows of m_pad floats, [tile_n][m_pad], put a warp's accesses
+// m_pad * 4 bytes apart: at m_pad 64 every 16-byte phase hit the same banks and
+// the exchange plus reduction took ~3.6 us of a 13.3 us GEMM on GB300.)  The
+// persistent kernel keeps the row layout.
+
 
 // Shared-memory matrix descriptor for a K-major bf16 tile whose rows are 128
 // bytes, written by TMA with 128-byte swizzling: 8-row swizzle atoms of 1024
@@ -542,11 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
                 if (ok && valid && !p.drop_mailbox) {
                     const uint32_t dst = ptx::mapa_shared(
-                        sbase + L.mailbox + ((rank - 1u) * kTileN + (uint32_t)row) * (M_PAD * 4u), 0);
+                        sbase + L.mailbox + (rank - 1u) * kSlotBytes + 16u * (uint32_t)row, 0);
                     const uint32_t rbar = ptx::mapa_shared(bar_reduce, 0);
 #pragma unroll
-                    for (int i = 0; i < M_PAD / 4; ++i)
-                        ptx::st_async_v4(dst + 16u * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                    for (int i = 0; i < M_PAD / 4; ++i)          // slot layout [m_pad / 4][tile_n] float4
+                        ptx::st_async_v4(dst + 16u * kTileN * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2],
+                                         acc[4 * i + 3]);
                 }
                 if (p.timeline != nullptr && etid == 0)
                     p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
@@ -560,14 +569,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::fence_acquire_shared_cluster();
                     if (valid && ok) {
-                        const float *box = reinterpret_cast<const float *>(smem + L.mailbox);
+                        const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
 #pragma unroll 1
                         for (int r = 1; r < SPLIT_K; ++r) {            // fixed rank order
-                            const float4 *src =
-                                reinterpret_cast<const float4 *>(box + ((r - 1) * kTileN + row) * M_PAD);
+                            const float4 *src = box + (r - 1) * (kSlotBytes / 16) + row;
 #pragma unroll
                             for (int i = 0; i < M_PAD / 4; ++i) {
-                                const float4 v = src[i];
+                                const float4 v = src[i * kTileN];
                                 acc[4 * i] += v.x;
                                 acc[4 * i + 1] += v.y;
                                 acc[4 * i + 2] += v.z;
@@ -612,10 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __all_sync(0xffffffffu, ok);
             __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
-            const float *box = reinterpret_cast<const float *>(smem + L.mailbox);
+            const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
             uint32_t dst = 0, rbar = 0;
             if (!owner) {
-                dst = ptx::mapa_shared(sbase + L.mailbox + ((rank - 1u) * kTileN + (uint32_t)row) * (M_PAD * 4u), 0);
+                dst = ptx::mapa_shared(sbase + L.mailbox + (rank - 1u) * kSlotBytes + 16u * (uint32_t)row, 0);
                 rbar = ptx::mapa_shared(bar_reduce, 0);
             }
 #pragma unroll 1
@@ -636,19 +644,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!owner) {
                     if (ok && valid && !p.drop_mailbox) {
 #pragma unroll
-                        for (int i = 0; i < kCh / 4; ++i)
-                            ptx::st_async_v4(dst + 4u * (uint32_t)c0 + 16u * i, rbar, acc[4 * i], acc[4 * i + 1],
-                                             acc[4 * i + 2], acc[4 * i + 3]);
+                        for (int i = 0; i < kCh / 4; ++i)          // slot layout [m_pad / 4][tile_n] float4
+                            ptx::st_async_v4(dst + 16u * kTileN * (uint32_t)(c0 / 4 + i), rbar, acc[4 * i],
+                                             acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
                     }
                 } else if (valid) {
                     if (SPLIT_K > 1 && ok) {
 #pragma unroll 1
                         for (int r = 1; r < SPLIT_K; ++r) {    // fixed rank order
-                            const float4 *src =
-                                reinterpret_cast<const float4 *>(box + ((r - 1) * kTileN + row) * M_PAD + c0);
+                            const float4 *src = box + (r - 1) * (kSlotBytes / 16) + (c0 / 4) * kTileN + row;
 #pragma unroll
                             for (int i = 0; i < kCh / 4; ++i) {
-                                const float4 v = src[i];
+                                const float4 v = src[i * kTileN];
                                 acc[4 * i] += v.x;
                                 acc[4 * i + 1] += v.y;
                                 acc[4 * i + 2] += v.z;
