@@ -206,6 +206,25 @@ __device__ __forceinline__ void load_accumulator(uint32_t taddr, float (&acc)[M_
     ptx::tmem_wait_ld();
 }
 
+// Both accumulators' columns [0, N) for this thread's lane, with one
+// tcgen05.wait::ld for all the loads: a[i] from taddr0 + i, b[i] from taddr1 + i.
+template <int N>
+__device__ __forceinline__ void load_accumulator_pair(uint32_t taddr0, uint32_t taddr1, float (&a)[N], float (&b)[N])
+{
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) {
+        uint32_t r0[8], r1[8];
+        ptx::tmem_ld_32x32b_x8(taddr0 + 8u * q, r0);
+        ptx::tmem_ld_32x32b_x8(taddr1 + 8u * q, r1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            a[8 * q + i] = __uint_as_float(r0[i]);
+            b[8 * q + i] = __uint_as_float(r1[i]);
+        }
+    }
+    ptx::tmem_wait_ld();
+}
+
 // One issuer's share of a stage's MMAs into the accumulator at tmem_d: of
 // every block's 4 K16 steps, issuer q of ISSUERS takes kk = q, q + ISSUERS, ...
 // `first` clears the accumulator with this issuer's first MMA of the stage.
@@ -523,8 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
                 float acc1[M_PAD];
-                load_accumulator<M_PAD>(tmem_base + lanes, acc);
-                load_accumulator<M_PAD>(tmem_base + lanes + kAcc1, acc1);
+                load_accumulator_pair<M_PAD>(tmem_base + lanes, tmem_base + lanes + kAcc1, acc, acc1);
 #pragma unroll
                 for (int i = 0; i < M_PAD; ++i)
                     acc[i] += acc1[i];                 // fixed order: accumulator 0 + accumulator 1
@@ -631,8 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float acc[kCh];
                 if (ok) {
                     float acc1[kCh];
-                    load_accumulator<kCh>(tmem_base + lanes + (uint32_t)c0, acc);
-                    load_accumulator<kCh>(tmem_base + lanes + kAcc1 + (uint32_t)c0, acc1);
+                    load_accumulator_pair<kCh>(tmem_base + lanes + (uint32_t)c0,
+                                               tmem_base + lanes + kAcc1 + (uint32_t)c0, acc, acc1);
 #pragma unroll
                     for (int i = 0; i < kCh; ++i)
                         acc[i] += acc1[i];             // fixed order: accumulator 0 + accumulator 1
