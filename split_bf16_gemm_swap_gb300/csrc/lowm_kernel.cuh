@@ -330,6 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_acc = bar_full + 16u * stages;              // accumulator complete (tcgen05.commit)
     const uint32_t bar_tmem_alloc = bar_acc + 8u;                  // two phases, 160 arrivals each
     const uint32_t bar_reduce = bar_acc + 16u;                     // owner's mailbox barrier
+    const uint32_t bar_reduce2 = bar_acc + 24u;                    // second half of the mailbox (two-phase)
+    // m_pad 64 splits each slot's float4 columns into two halves with a
+    // barrier each, so the owner reduces and stages the first half while the
+    // second is still arriving (GB300, M64 N6144 K4096: 11.55 -> 11.31 us; at
+    // m_pad 32 the 8 KiB slot gains nothing: 10.09 -> 10.14 us).
+    constexpr bool kTwoPhase = SPLIT_K > 1 && M_PAD == 64;
+    constexpr int kHalf4 = M_PAD / 8;                              // float4 columns in the first half
     const uint32_t tmem_slot = sbase + L.tmem_slot;
 
     // ---------------------------------------------------------------- prologue
@@ -341,8 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_acc, 2);                        // each issuer's final commit
         ptx::mbar_init(bar_tmem_alloc, kTmemBarArrivals);
         ptx::mbar_init(bar_reduce, 1);
-        if (SPLIT_K > 1 && rank == 0)     // arm the mailbox: every peer sends one full partial tile
-            ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes);
+        ptx::mbar_init(bar_reduce2, 1);
+        if (SPLIT_K > 1 && rank == 0) {   // arm the mailbox: every peer sends one full partial tile
+            if (kTwoPhase) {
+                ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 2);
+                ptx::mbar_arrive_expect_tx(bar_reduce2, (SPLIT_K - 1) * kSlotBytes / 2);
+            } else {
+                ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes);
+            }
+        }
         ptx::fence_mbarrier_init_cluster();
         ptx::fence_proxy_async_shared();          // the inits before this thread's own TMA copies below
     }
@@ -570,11 +584,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dst = ptx::mapa_shared(
                         sbase + L.mailbox + (rank - 1u) * kSlotBytes + 16u * (uint32_t)row, 0);
                     const uint32_t rbar = ptx::mapa_shared(bar_reduce, 0);
+                    const uint32_t rbar2 = kTwoPhase ? ptx::mapa_shared(bar_reduce2, 0) : rbar;
 #pragma unroll
                     for (int i = 0; i < M_PAD / 4; ++i)          // slot layout [m_pad / 4][tile_n] float4
-                        ptx::st_async_v4(dst + 16u * kTileN * i, rbar, acc[4 * i], acc[4 * i + 1], acc[4 * i + 2],
-                                         acc[4 * i + 3]);
+                        ptx::st_async_v4(dst + 16u * kTileN * i, (kTwoPhase && i >= kHalf4) ? rbar2 : rbar, acc[4 * i],
+                                         acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
                 }
+                if (p.timeline != nullptr && etid == 0)
+                    p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
+            } else if constexpr (kTwoPhase) {
+                // Owner, two-phase: per half, the relaxed cluster-scope wait and the
+                // acquire fence, then the rank-ordered sum of that half's columns
+                // (each element's order is the one-phase order), bf16 into staging.
+                __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
+                const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    bool okh = ok;
+                    if (!wait_bounded<true>(h == 0 ? bar_reduce : bar_reduce2, 0, p.reduce_timeout_ns)) {
+                        record_error(p, kErrReduce);
+                        okh = false;
+                    }
+                    ptx::fence_acquire_shared_cluster();
+                    if (valid) {
+                        if (okh) {
+#pragma unroll 1
+                            for (int r = 1; r < SPLIT_K; ++r) {        // fixed rank order
+                                const float4 *src = box + (r - 1) * (kSlotBytes / 16) + row;
+#pragma unroll
+                                for (int i = h * kHalf4; i < (h + 1) * kHalf4; ++i) {
+                                    const float4 v = src[i * kTileN];
+                                    acc[4 * i] += v.x;
+                                    acc[4 * i + 1] += v.y;
+                                    acc[4 * i + 2] += v.z;
+                                    acc[4 * i + 3] += v.w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int m = h * (M_PAD / 2); m < (h + 1) * (M_PAD / 2); ++m)
+                            stage_out[m * kTileN + row] = __float2bfloat16_rn(acc[m]);
+                        if (p.c_f32 != nullptr) {
+#pragma unroll
+                            for (int m = h * (M_PAD / 2); m < (h + 1) * (M_PAD / 2); ++m)
+                                if (m < p.M && n0 + row < p.N)
+                                    p.c_f32[(size_t)m * p.N + n0 + row] = acc[m];
+                        }
+                    }
+                }
+                ptx::named_barrier_sync(1, kEpilogueThreads);
+                store_tile<kTileN>(p, stage_out, n0, etid);
                 if (p.timeline != nullptr && etid == 0)
                     p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
             } else {

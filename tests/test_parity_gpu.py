@@ -231,6 +231,22 @@ def test_a_dropped_mailbox_times_out_and_the_context_survives():
     check(A, W, 2)
 
 
+@pytest.mark.parametrize("M,split_k", [(64, 2), (64, 4), (32, 2)])
+def test_a_dropped_two_phase_mailbox_times_out(M, split_k):
+    # m_pad 64 waits on two mailbox halves (m_pad 32 on one); every bounded
+    # wait must run out, report the mailbox bit, and leave a working context.
+    N, K = 256, 1024
+    A, W = inputs.make_problem(M, N, K, seed=5)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    st = lowm.lowm_gemm_bf16_debug(Ad, Wd, C, M, N, K, split_k, None, drop_mailbox=1,
+                                   reduce_timeout_ns=20_000_000)
+    assert st == lowm.LOWM_OK
+    st, detail = lowm.lowm_gemm_sync_status()
+    assert st == lowm.LOWM_ERR_TIMEOUT and detail == (1 << 8), (st, hex(detail))
+    check(A, W, split_k)
+
+
 def test_w_before_pdl_wait_flag_keeps_the_chain_correct():
     # W is never written by the preceding kernel here, so the flag's promise holds;
     # A is the previous GEMM's output and must still be read after the wait.
