@@ -273,3 +273,12 @@ def test_the_header_is_c99_and_links_against_the_library(L, tmp_path):
     want = [t[k] for k in ("tile_n", "m_pad", "split_k", "kb_per_stage", "stages", "ctas", "mma_issuers",
                            "w_prefetch_stages")]
     assert [int(x) for x in out.stdout.split()] == want
+
+
+@pytest.mark.parametrize("M", [96, 128])
+def test_m_pad_128_tactic_is_the_measured_best(L, M):
+    # GB300 sweep at N6144 K4096: split_k 1, 64-column tiles, 4 x 2 ring
+    # (15.8 us) beat every split-2 and 128-column choice (19.8-53 us).
+    st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 0)
+    assert st == lowm.LOWM_OK
+    assert (t["tile_n"], t["split_k"], t["kb_per_stage"], t["stages"], t["ctas"]) == (64, 1, 4, 2, 96)
