@@ -61,7 +61,10 @@ typedef enum {
  *                mapped onto the tensor core's M, the tiny M onto its N)
  *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64 or 128);
  *                rows M..m_pad-1 are zero-filled by the TMA unit and never stored
- *   split_k      CTAs per cluster along K (1, 2, 4 or 8)
+ *   split_k      CTAs per cluster along K (1, 2, 3, 4 or 8).  K is cut into
+ *                stages of kb_per_stage 64-wide blocks and rank r takes
+ *                stages [r*T/split_k, (r+1)*T/split_k) of the T in all, so
+ *                the ranks' shares differ by at most one stage
  *   stages       depth of the shared-memory ring between the TMA producer and the MMA warp
  *   block_k      K elements per block (64: one 128-byte swizzle row of bf16)
  *   tiles        ceil(N / tile_n) output tiles (the last may be partial)
@@ -77,9 +80,11 @@ typedef enum {
  *                gets the same number of tiles, tiles_per_cluster)
  *   tiles_per_cluster  ceil(tiles / num_clusters)
  *   kb_per_stage 64-wide K blocks per ring stage, fetched by one 3-D TMA
- *                copy of W and one of A (the largest of 4, 2, 1 dividing the
- *                rank's block count): a copy has a fixed per-CTA cost, so
- *                larger copies are what let one CTA stream its share of HBM
+ *                copy of W and one of A (the largest of 8, 4, 2, 1 that
+ *                divides the rank's block count and whose two-stage ring
+ *                fits both the per-SM shared-memory budget and 160 KiB of
+ *                W): a copy has a fixed per-CTA cost, so larger copies are
+ *                what let one CTA stream its share of HBM
  *   mma_issuers  threads issuing tcgen05.mma per CTA: 2 for the one-tile
  *                kernel (one takes the even, the other the odd 16-wide K steps
  *                of every stage, each into its own TMEM accumulator; the
@@ -89,6 +94,17 @@ typedef enum {
  *   w_prefetch_stages  ring stages of W requested before the
  *                programmatic-dependency wait under
  *                LOWM_FLAG_W_BEFORE_PDL_WAIT (0 without the flag)
+ *   mbox_in_ring 1: the split-K mailbox and the output staging share the
+ *                owner's ring memory, which they use only after the owner's
+ *                last MMA has completed (the owner then tells each peer that
+ *                its mailbox is open); a CTA needs max(ring, mailbox) bytes of
+ *                shared memory instead of their sum.  0: the mailbox sits
+ *                after the ring.
+ *   l2_prefetch_stages  stages of W the producer requests into L2 (TMA
+ *                prefetch, no shared-memory destination) ahead of its newest
+ *                ring load, so that one more stage of W is in flight than the
+ *                ring's shared memory holds (0: none; the persistent kernel
+ *                uses none)
  * The pages' shipped tactic reads as (tile_n 64, m_pad 8, split_k 2, stages 10)
  * ("Fix two synchronization gaps ...", Hardware verification).
  */
@@ -97,24 +113,27 @@ typedef struct {
     int tiles, num_clusters, ctas, smem_bytes, pdl;
     int persistent, tiles_per_cluster, kb_per_stage;
     int mma_issuers, w_prefetch_stages;
+    int mbox_in_ring, l2_prefetch_stages;
 } lowm_tactic_t;
 
 /*
  * C = A . W^T on `stream`: the low-M split-K GEMM of the PR page
  * (Description; the launch shape of Hardware verification: clusters of
  * split_k CTAs along the output columns, programmatic dependent launch on).
- *   M        1..128 (M > 64 pads to m_pad 128; those shapes run split_k 1, 2
- *            or 4 with 64-column tiles, 1 or 2 with 128-column tiles)
+ *   M        1..128 (M > 64 pads to m_pad 128; those shapes run split_k 1, 2,
+ *            3 or 4 with 64-column tiles, 1, 2 or 3 with 128-column tiles)
  *   N        any positive value; when N is not a multiple of tile_n the last
  *            tile is partial (the TMA unit zero-fills W rows >= N and the
  *            epilogue stores only columns < N; 16-byte stores when N % 8 == 0,
  *            element stores otherwise)
- *   K        a positive multiple of split_k * 64
- *   split_k  0 (let the tactic table choose), 1, 2, 4 or 8
+ *   K        a positive multiple of 64 with K / 64 >= split_k (every rank
+ *            gets a non-empty share of K, the condition the TMEM-release
+ *            argument of the PR page's Description relies on)
+ *   split_k  0 (let the tactic table choose), 1, 2, 3, 4 or 8
  *   A, W, C  device pointers, 16-byte aligned; C must not overlap A or W
  * Returns LOWM_OK once the kernel is enqueued.  Errors, all before anything
  * is enqueued: LOWM_ERR_INVALID_ARGUMENT (a NULL pointer, M, N or K <= 0,
- * split_k outside {0, 1, 2, 4, 8}, C overlapping A or W),
+ * split_k outside {0, 1, 2, 3, 4, 8}, C overlapping A or W),
  * LOWM_ERR_MISALIGNED, LOWM_ERR_UNSUPPORTED_SHAPE (a rule above, or no
  * tactic whose shared memory fits), LOWM_ERR_UNSUPPORTED_ARCH; a failed
  * launch returns LOWM_ERR_CUDA.  The result is deterministic: the same
@@ -194,13 +213,27 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
  *   stages           0: tactic default; else the ring depth to use (>= 2)
  *   drop_mailbox     1: the non-owner ranks skip their mailbox publication, so
  *                    the owner's mailbox wait runs out (a dropped message, to
- *                    test the timeout path); the output is then undefined
+ *                    test the timeout path); the output is then undefined.
+ *                    After a mailbox wait runs out, the owner waits once more
+ *                    with the same bound before it exits, so that a peer that
+ *                    is only slow lands its partial tile while the owner's
+ *                    shared memory still exists; a peer slower than both
+ *                    bounds could still write after the owner exited, which
+ *                    CUDA leaves undefined, so treat LOWM_ERR_TIMEOUT as
+ *                    fatal for the outputs of the launches it reports.
  *   reduce_timeout_ns 0: default (2 s); else the bound on the owner's
  *                    mailbox wait.  Every other wait keeps its 2 s bound.
- *   probes           NULL, or device u64[2 * ctas]: per CTA (by linear CTA
+ *   probes           NULL, or device u64[3 * ctas]: per CTA (by linear CTA
  *                    index) [0] = latest %globaltimer after any epilogue
- *                    thread's tcgen05.wait::ld, [1] = %globaltimer just before
- *                    tcgen05.dealloc.  Zero-initialise before the launch.
+ *                    thread's last tcgen05.wait::ld, [1] = %globaltimer just
+ *                    before tcgen05.dealloc, [2] = the ordering tickets the
+ *                    MMA warp saw just before tcgen05.dealloc: each of the 4
+ *                    epilogue warps takes one from a shared counter after its
+ *                    last tcgen05.wait::ld and before its release arrival, so
+ *                    4 means every epilogue load was complete when TMEM was
+ *                    freed (an exact order, unlike two clock reads that can
+ *                    fall in the same timer tick).  Zero-initialise before
+ *                    the launch.
  *   c_f32            NULL, or device float[M*N]: the fp32 sums before the bf16
  *                    rounding (written by the owner rank)
  *   flags            launch flags as for lowm_gemm_bf16_ex (LOWM_FLAG_*)

@@ -18,6 +18,8 @@ KernelFn by_split(int split_k, bool persistent)
     switch (split_k) {
     case 1: return instance<MP, 1>(persistent);
     case 2: return instance<MP, 2>(persistent);
+    case 3:   // uneven K split; one-tile schedule only
+        return persistent ? nullptr : reinterpret_cast<KernelFn>(&lowm_splitk_kernel<128, MP, 3>);
     case 4: return instance<MP, 4>(persistent);
     case 8: return instance<MP, 8>(persistent);
     default: return nullptr;

@@ -129,9 +129,21 @@ int m_pad_of(int M)
     return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
 }
 
-int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs)
+int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs, bool alias = false)
 {
-    return (int)lowm::make_smem_layout(tile_n, m_pad, split_k, stages, kbs, bufs).bytes;
+    return (int)lowm::make_smem_layout(tile_n, m_pad, split_k, stages, kbs, bufs, alias).bytes;
+}
+
+// May a stage of `kbs` K blocks tile a K of `kb_total` blocks split `split_k`
+// ways?  kbs must divide the K blocks, every rank must get at least one stage,
+// and when split_k divides the blocks evenly the ranks' shares stay equal.
+bool kbs_tiles_k(int kbs, int kb_total, int split_k)
+{
+    if (kb_total % kbs != 0 || kb_total / kbs < split_k)
+        return false;
+    if (kb_total % split_k == 0 && (kb_total / split_k) % kbs != 0)
+        return false;
+    return true;
 }
 
 // Ring shape (K blocks per stage x stages) for a launch of `ctas` CTAs on
@@ -155,7 +167,7 @@ struct Ring {
 
 constexpr int kMaxRingBytes = 160 * 1024;
 
-Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, int sms, int bufs)
+Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int sms, int bufs, bool alias = false)
 {
     const int per_sm_one_wave = (ctas + std::max(1, sms) - 1) / std::max(1, sms);
     const int per_sm = per_sm_one_wave <= 4 ? std::max(1, per_sm_one_wave) : (split_k == 1 ? 3 : 5);
@@ -163,8 +175,8 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, 
     int force_kbs = env_int("LOWM_KB_PER_STAGE", 0);
     if (force_kbs != 1 && force_kbs != 2 && force_kbs != 4 && force_kbs != 8)
         force_kbs = 0;
-    if (force_kbs && kb_per_rank % force_kbs != 0)
-        force_kbs = 0;                                 // a forced value that does not divide is ignored
+    if (force_kbs && !kbs_tiles_k(force_kbs, kb_total, split_k))
+        force_kbs = 0;                                 // a forced value that does not tile K is ignored
     const int force_st = env_int("LOWM_STAGES", 0);
     auto ring_bytes = [&](int kbs, int st) { return st * kbs * (int)lowm::w_block_bytes(tile_n); };   // W bytes
     int kbs = 1;
@@ -172,7 +184,7 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, 
         kbs = force_kbs;
     } else {
         for (int b = 8; b >= 1; b /= 2)
-            if (kb_per_rank % b == 0 && footprint(tile_n, m_pad, split_k, 2, b, bufs) <= budget &&
+            if (kbs_tiles_k(b, kb_total, split_k) && footprint(tile_n, m_pad, split_k, 2, b, bufs, alias) <= budget &&
                 ring_bytes(b, 2) <= kMaxRingBytes) {
                 kbs = b;
                 break;
@@ -182,37 +194,108 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_per_rank, int ctas, 
     if (force_st >= 2) {
         st = force_st;
     } else {
-        while (st < 32 && footprint(tile_n, m_pad, split_k, st + 1, kbs, bufs) <= budget &&
+        while (st < 32 && footprint(tile_n, m_pad, split_k, st + 1, kbs, bufs, alias) <= budget &&
                ring_bytes(kbs, st + 1) <= kMaxRingBytes)
             ++st;
     }
     return Ring{kbs, st};
 }
 
+// K is split in whole stages: every rank needs at least one 64-wide K block.
 bool shape_ok(int M, int N, int K, int split_k)
 {
-    return M >= 1 && M <= 128 && N > 0 && K > 0 && K % (split_k * lowm::kBlockK) == 0;
+    return M >= 1 && M <= 128 && N > 0 && K > 0 && K % lowm::kBlockK == 0 && K / lowm::kBlockK >= split_k;
 }
 
-// split_k = 0: the smallest split (1, 2, 4, 8) that keeps the K loop non-empty
-// and gives at least one CTA per SM (counted in 64-column tiles), preferring
-// fewer cluster reductions; never a split whose mailbox leaves no room for a
-// two-stage ring (m_pad 128 stops at split_k 4).  At m_pad 128 every split
-// costs a tile_n x 128 fp32 mailbox slot and ring depth, so one CTA on half
-// the SMs is enough (M128 N6144 K4096 on GB300: split_k 1 15.8 us, 2 25.6 us).
+// Tile width (the MMA's M), given the split.  128 columns when N is a
+// multiple of 128, the 64-column grid would not fit the GPU at one CTA per SM
+// while the 128-column grid does, and each 128-column CTA streams at most 1
+// MiB of W (a short GEMM, where per-GEMM fixed costs weigh most); 64 columns
+// otherwise.  Measured on GB300 with the one-stage L2 prefetch: one CTA per
+// SM streaming a 128-column tile through a ~160 KiB ring is fastest where the
+// 64-column grid overflows the SMs (N6144 K4096 split_k 2: M4 9.43 us against
+// 10.14 with 64 columns, M32 9.59 against 10.32, M64 10.92, M128 14.08
+// against 15.8), while a 64-column grid that already fits, a grid that
+// overflows at both widths, or a long stream per CTA is faster on 64 columns
+// (M4 N2304 K12288 split_k 4: 9.95 against 11.17 us; M4 N49152 K4096: 59.9
+// against 63.4 us; M16 N6144 K32768: 64.2 us at split_k 4 against 69.2 us on
+// 128 columns at split_k 2).  At m_pad 8 a 128-column tile pads the MMA's N
+// to 16 (zero rows from the TMA unit, no extra HBM bytes).  LOWM_TILE_N = 64
+// / 128 overrides when the shape allows it (tuning).
+constexpr double kShortStreamBytes = 1024.0 * 1024.0;   // W bytes per 128-column CTA
+
+int choose_tile_n(int N, int K, int split_k, int sms)
+{
+    const int force = env_int("LOWM_TILE_N", 0);
+    if (force == 128 && N >= 128)
+        return 128;
+    if (force == 64)
+        return 64;
+    const long long c64 = (long long)((N + 63) / 64) * split_k, c128 = (long long)((N + 127) / 128) * split_k;
+    const double per_cta = 2.0 * N * (double)K / (double)c128;
+    return (N % 128 == 0 && c64 > sms && c128 <= sms && per_cta <= kShortStreamBytes) ? 128 : 64;
+}
+
+int m_pad_for(int M, int tile_n)
+{
+    const int mp = m_pad_of(M);
+    return tile_n == 128 && mp < 16 ? 16 : mp;          // MMA M = 128 needs N a multiple of 16
+}
+
+// The split-K mailbox shares the drained ring (see make_smem_layout) for
+// split_k 3 and for m_pad 128, whose 32-64 KiB slots would otherwise take the
+// ring's room (M128 N6144 K4096 split_k 2 on 128-column tiles: 14.4 us
+// against 16.4 us with the mailbox next to the ring).  LOWM_MBOX_IN_RING =
+// 0 / 1 overrides (tuning).
+bool choose_alias(int m_pad, int split_k)
+{
+    bool alias = split_k == 3 || (m_pad == 128 && split_k > 1);
+    const int force = env_int("LOWM_MBOX_IN_RING", -1);
+    if (force == 0 || force == 1)
+        alias = force == 1;
+    return alias && split_k > 1;
+}
+
+KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent);
+
+// A split whose kernel instance exists, whose K loop is non-empty and even,
+// and whose mailbox fits next to (or inside) a two-stage ring.
+bool split_usable(int M, int N, int K, int sk, int sms)
+{
+    if (K % (sk * lowm::kBlockK) != 0)
+        return false;
+    const int tile_n = choose_tile_n(N, K, sk, sms);
+    const int mp = m_pad_for(M, tile_n);
+    return kernel_for(tile_n, mp, sk, false) &&
+           footprint(tile_n, mp, sk, 2, 1, 1, choose_alias(mp, sk)) <= kMaxSmemPerCta;
+}
+
+// split_k = 0.  A short GEMM (at most 1 MiB of W per 128-column CTA) takes the
+// smallest even split that gives between half and all of the SMs one
+// 128-column CTA each (M4..M128 N6144 K4096: split_k 2, 96 CTAs, 9.4-14.1 us,
+// against 9.9 us at split_k 4 on 192 CTAs); otherwise the smallest even split
+// of 64-column tiles that fills 90 % of the SMs (M4 N2304 K12288: split_k 4 on
+// 144 CTAs, 10.07 us, against 11.08 us at split_k 8), where clusters of 8
+// measured slowest.  The K loop stays non-empty and the mailbox fits.
 int choose_split_k(int M, int N, int K, int sms)
 {
-    const int tiles = (N + 63) / 64;
-    const int mp = m_pad_of(M);
-    const int want = mp == 128 ? (sms + 1) / 2 : sms;
+    if (N % 128 == 0) {
+        const int tiles128 = N / 128;
+        for (int sk = 1; sk <= 4; sk *= 2) {
+            const long long c = (long long)tiles128 * sk;
+            if (c > sms || !split_usable(M, N, K, sk, sms))
+                break;
+            if (2 * c >= sms && 2.0 * N * (double)K / (double)c <= kShortStreamBytes)
+                return sk;
+        }
+    }
+    const int tiles64 = (N + 63) / 64;
     int best = 0;
     for (int sk = 1; sk <= 8; sk *= 2) {
-        if (K % (sk * lowm::kBlockK) != 0)
-            break;
-        if (footprint(64, mp, sk, 2, 1, 1) > kMaxSmemPerCta || (mp == 128 && sk > 4))
+        if (!split_usable(M, N, K, sk, sms))
             break;
         best = sk;
-        if (tiles * sk >= want)
+        if (10LL * tiles64 * sk >= 9LL * sms)
             break;
     }
     return best;
@@ -221,6 +304,8 @@ int choose_split_k(int M, int N, int K, int sms)
 // ------------------------------------------------------------------ kernels
 KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent)
 {
+    if (persistent && sk == 3)
+        return nullptr;                                 // the persistent schedule splits K evenly (1, 2, 4, 8)
     if (m_pad == 128)
         return persistent ? nullptr : lowm::kernel_mpad128(tile_n, sk);
     if (tile_n == 64)
@@ -318,63 +403,52 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
 {
     if (M <= 0 || N <= 0 || K <= 0 || split_k < 0)
         return LOWM_ERR_INVALID_ARGUMENT;
-    if (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8)
+    if (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 3 && split_k != 4 && split_k != 8)
         return LOWM_ERR_INVALID_ARGUMENT;
     if (split_k == 0)
         split_k = choose_split_k(M, N, K, sms > 0 ? sms : 152);
     if (split_k == 0 || !shape_ok(M, N, K, split_k))
         return LOWM_ERR_UNSUPPORTED_SHAPE;
-    const int kbr = K / (split_k * lowm::kBlockK);
+    const int kbt = K / lowm::kBlockK;                  // K blocks in all
     if (stages_override == 1)
         return LOWM_ERR_INVALID_ARGUMENT;
     const int nsm = sms > 0 ? sms : 152;
-    // Tile width.  128-column tiles (MMA M = 128: every epilogue lane holds a
-    // row, and each W copy is twice as large) measured faster for m_pad 16
-    // and 64 and slower for m_pad 8 and 32 (M 8..64 sweep at N6144 K4096 and
-    // M16 N6144 K32768 on GB300).  LOWM_TILE_N = 64 / 128 overrides when the
-    // shape allows it (tuning).
-    int tile_n = 64;
-    {
-        const int force = env_int("LOWM_TILE_N", 0);
-        const bool can128 = N % 128 == 0;
-        const int mp = m_pad_of(M);
-        if (force == 128 && N >= 128)
-            tile_n = 128;
-        else if (force != 64 && can128 && (mp == 16 || mp == 64))
-            tile_n = 128;
-    }
-    int m_pad = m_pad_of(M);
-    if (tile_n == 128 && m_pad < 16)
-        m_pad = 16;                                     // MMA M = 128 needs N a multiple of 16
-    // The persistent schedule is opt-in (LOWM_PERSISTENT=1).
-    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad != 128;   // no persistent m_pad 128 instance
+    int tile_n = choose_tile_n(N, K, split_k, nsm);
+    int m_pad = m_pad_for(M, tile_n);
+    // The persistent schedule is opt-in (LOWM_PERSISTENT=1); it splits K evenly.
+    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad != 128 &&   // no persistent m_pad 128 instance
+                      kbt % split_k == 0 && split_k != 3;
+    bool alias = choose_alias(m_pad, split_k);
     int tiles = (N + tile_n - 1) / tile_n;            // the last tile may be partial
     int clusters = tiles;
-    Ring ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
+    Ring ring = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, alias);
     if (stages_override >= 2)
         ring.stages = stages_override;
-    int fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1);
-    if (fp > kMaxSmemPerCta && tile_n == 128) {
-        // e.g. m_pad 64 with split_k 8: the 128-column mailbox does not fit; use 64 columns
+    int fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1, alias);
+    if (tile_n == 128 && (fp > kMaxSmemPerCta || !kernel_for(tile_n, m_pad, split_k, false))) {
+        // e.g. m_pad 64 with split_k 8: the 128-column mailbox does not fit, or
+        // m_pad 128 with split_k 4: no 128-column instance; use 64 columns
         tile_n = 64;
         m_pad = m_pad_of(M);
+        alias = choose_alias(m_pad, split_k);
         tiles = (N + tile_n - 1) / tile_n;
         clusters = tiles;
-        ring = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 1);
+        ring = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, alias);
         if (stages_override >= 2)
             ring.stages = stages_override;
-        fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1);
+        fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1, alias);
     }
     if (fp > kMaxSmemPerCta || !kernel_for(tile_n, m_pad, split_k, false))
         return LOWM_ERR_UNSUPPORTED_SHAPE;
     int smem = full_smem ? kMaxSmemPerCta : fp;
     if (persistent) {
         // Size the persistent grid for the CTAs that fit at the chosen footprint.
-        Ring pr = choose_ring(tile_n, m_pad, split_k, kbr, tiles * split_k, nsm, 2);
+        Ring pr = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 2);
         if (stages_override >= 2)
             pr.stages = stages_override;
         const int fp2 = footprint(tile_n, m_pad, split_k, pr.stages, pr.kbs, 2);
         if (fp2 <= kMaxSmemPerCta) {
+            alias = false;
             ring = pr;
             fp = fp2;
             smem = full_smem ? kMaxSmemPerCta : fp;
@@ -404,6 +478,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     t->tiles_per_cluster = (tiles + clusters - 1) / clusters;
     t->kb_per_stage = kbs;
     t->mma_issuers = persistent ? 1 : 2;
+    t->mbox_in_ring = alias ? 1 : 0;
     // W stages requested ahead of the programmatic-dependency wait when the
     // caller promises that the preceding kernel does not write W: the whole
     // ring, except for rings of three or more 64-column stages (M <= 8 at
@@ -416,6 +491,17 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     if (force_wpf >= 0)
         wpf = std::min(force_wpf, stages);
     t->w_prefetch_stages = wpf;
+    // W stages requested into L2 ahead of the newest ring load: one measured
+    // fastest for every workload (GB300, interleaved repeats: M4 N6144 K4096
+    // split_k 2 10.49 -> 10.15 us, M4 N2304 K12288 split_k 4 10.73 -> 9.95,
+    // M64 11.37 -> 10.93, M128 14.51 -> 14.05, M4 N49152 60.78 -> 59.95);
+    // two or more were slower than one almost everywhere.  LOWM_L2_PREFETCH
+    // overrides (tuning).
+    int l2pf = persistent ? 0 : 1;
+    const int force_l2pf = env_int("LOWM_L2_PREFETCH", -1);
+    if (force_l2pf >= 0 && !persistent)
+        l2pf = force_l2pf;
+    t->l2_prefetch_stages = l2pf;
     return LOWM_OK;
 }
 
@@ -536,10 +622,13 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     p.stages = t.stages;
     p.kb_per_rank = K / (t.split_k * lowm::kBlockK);
     p.kb_per_stage = t.kb_per_stage;
+    p.stages_total = K / (lowm::kBlockK * t.kb_per_stage);
+    p.mbox_in_ring = t.mbox_in_ring ? 1u : 0u;
     p.num_tiles = t.tiles;
     p.timeout_ns = lowm::kDefaultTimeoutNs;
     p.reduce_timeout_ns = lowm::kDefaultTimeoutNs;
     p.w_prefetch_stages = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) ? (uint32_t)t.w_prefetch_stages : 0u;
+    p.l2_prefetch_stages = (uint32_t)t.l2_prefetch_stages;
     if (dbg) {
         p.stall_warp_mask = dbg->stall_warp_mask;
         p.stall_rank_mask = dbg->stall_rank_mask;
@@ -583,9 +672,9 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     if (std::getenv("LOWM_LOG"))
         std::fprintf(stderr,
                      "lowm: M%d N%d K%d -> tile_n %d m_pad %d split_k %d stages %d x %d blocks ctas %d smem %d "
-                     "persistent %d\n",
+                     "persistent %d mbox_in_ring %d\n",
                      M, N, K, t.tile_n, t.m_pad, t.split_k, t.stages, t.kb_per_stage, t.ctas, t.smem_bytes,
-                     t.persistent);
+                     t.persistent, t.mbox_in_ring);
     if (cudaLaunchKernelEx(&cfg, fn, map_a, map_w, p) != cudaSuccess)
         return LOWM_ERR_CUDA;
     return LOWM_OK;
@@ -639,7 +728,7 @@ const char *lowm_status_string(lowm_status_t s)
     switch (s) {
     case LOWM_OK: return "ok";
     case LOWM_ERR_INVALID_ARGUMENT: return "invalid argument";
-    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=128, N>=1, K%(split_k*64)==0, and a split-K mailbox that fits)";
+    case LOWM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need 1<=M<=128, N>=1, K a multiple of 64 with K/64>=split_k, and a split-K mailbox that fits)";
     case LOWM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case LOWM_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103 (GB300)";
     case LOWM_ERR_CUDA: return "CUDA runtime error";

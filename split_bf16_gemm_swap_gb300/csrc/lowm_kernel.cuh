@@ -69,6 +69,8 @@ __host__ __device__ constexpr uint32_t w_block_bytes(int tile_n)   // one tile_n
     return (uint32_t)tile_n * kBlockK * 2u;
 }
 constexpr uint32_t kTmemBarArrivals = 32 + kEpilogueThreads;
+constexpr uint32_t kTicketOffset = 8;      // byte offset of the ordering-ticket counter from SmemLayout::tmem_slot
+constexpr int kProbeWords = 3;             // probes per CTA: [t_ld, t_dealloc, tickets seen at dealloc]
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;     // 2 s per wait on another party
 constexpr uint64_t kDrainTimeoutNs = 2000000000ull;       // 2 s for this CTA's own copies / MMAs in flight
 
@@ -83,6 +85,7 @@ enum : uint32_t {
     kErrEpiTmemPhase0 = 1u << 6,
     kErrEpiAccFull = 1u << 7,
     kErrReduce = 1u << 8,
+    kErrMailboxOpen = 1u << 9,     // a peer's wait for the owner's "mailbox open" signal (ring-aliased mailbox)
 };
 
 struct KernelParams {
@@ -90,8 +93,11 @@ struct KernelParams {
     unsigned int *status;   // device status word (bits of the waits that gave up), owned by the library
     int M, N, K;
     int stages;             // ring depth
-    int kb_per_stage;       // 64-wide K blocks per stage (divides kb_per_rank)
-    int kb_per_rank;        // 64-wide K blocks per cluster rank
+    int kb_per_stage;       // 64-wide K blocks per stage
+    int kb_per_rank;        // 64-wide K blocks per cluster rank (persistent kernel: an even split)
+    int stages_total;       // K / (64 * kb_per_stage): rank r of lowm_splitk_kernel takes stages
+                            // [r * stages_total / split_k, (r + 1) * stages_total / split_k)
+    uint32_t mbox_in_ring;  // 1: the mailbox and the output staging alias the (drained) ring
     int num_tiles;          // ceil(N / tile_n) (the persistent kernel walks them; the other kernel has one per cluster)
     uint64_t timeout_ns;    // bound on every wait for another party
     uint64_t reduce_timeout_ns;   // bound on the owner's mailbox wait
@@ -100,7 +106,8 @@ struct KernelParams {
     uint32_t drop_mailbox;  // non-owner ranks skip their publication (the owner's wait runs out)
     uint32_t w_prefetch_stages;   // stages of W requested before the programmatic-dependency wait
                                   // (0 unless the caller promised the preceding kernel does not write W)
-    unsigned long long *probes;
+    uint32_t l2_prefetch_stages;  // W stages requested into L2 ahead of the newest ring load (0: none)
+    unsigned long long *probes;     // [kProbeWords * ctas], see lowm_debug_opts_t
     float *c_f32;
     unsigned long long *timeline;   // [4 * ctas]: prologue end, first / last full stage, epilogue end
 };
@@ -112,9 +119,20 @@ struct SmemLayout {
 };
 
 // `bufs` = 1 for the one-tile-per-cluster kernel, 2 for the persistent kernel
-// (double-buffered mailbox and output staging).
+// (double-buffered mailbox and output staging).  `mbox_in_ring` (one-tile
+// kernel only) places the mailbox, then the output staging, at the start of
+// the ring instead of after it: both are used only once the ring is drained
+// (the owner stages its output after its last MMA has completed, and a peer
+// writes the owner's mailbox only after the owner has said so; see
+// lowm_splitk_kernel), so a split-K CTA needs max(ring, mailbox + staging)
+// bytes rather than their sum.
+__host__ __device__ inline uint32_t ring_bytes_of(int tile_n, int m_pad, int stages, int kb_per_stage)
+{
+    return (uint32_t)stages * (uint32_t)kb_per_stage * (w_block_bytes(tile_n) + (uint32_t)m_pad * 128u);
+}
+
 __host__ __device__ inline SmemLayout make_smem_layout(int tile_n, int m_pad, int split_k, int stages,
-                                                       int kb_per_stage, int bufs = 1)
+                                                       int kb_per_stage, int bufs = 1, bool mbox_in_ring = false)
 {
     SmemLayout L;
     uint32_t off = 0;
@@ -122,13 +140,22 @@ __host__ __device__ inline SmemLayout make_smem_layout(int tile_n, int m_pad, in
     off += (uint32_t)stages * (uint32_t)kb_per_stage * w_block_bytes(tile_n);
     L.a = off;                                            // [stages][kb_per_stage][m_pad][64 k]; m_pad*128 % 1024 == 0
     off += (uint32_t)stages * (uint32_t)kb_per_stage * (uint32_t)m_pad * 128u;
-    L.mailbox = off;                                      // [bufs][split_k-1] slots of tile_n x m_pad fp32 (*)
-    off += (uint32_t)bufs * (uint32_t)(split_k - 1) * (uint32_t)tile_n * (uint32_t)m_pad * 4u;
-    L.out = off;                                          // [bufs][m_pad][tile_n] bf16 staging for C
-    off += (uint32_t)bufs * (uint32_t)m_pad * (uint32_t)tile_n * 2u;
+    const uint32_t mbox_bytes = (uint32_t)bufs * (uint32_t)(split_k - 1) * (uint32_t)tile_n * (uint32_t)m_pad * 4u;
+    const uint32_t out_bytes = (uint32_t)bufs * (uint32_t)m_pad * (uint32_t)tile_n * 2u;
+    if (mbox_in_ring) {
+        L.mailbox = L.w;                                  // [split_k-1] slots of tile_n x m_pad fp32 (*)
+        L.out = L.w + mbox_bytes;                         // [m_pad][tile_n] bf16 staging for C
+        if (off < mbox_bytes + out_bytes)
+            off = mbox_bytes + out_bytes;
+    } else {
+        L.mailbox = off;                                  // [bufs][split_k-1] slots of tile_n x m_pad fp32 (*)
+        off += mbox_bytes;
+        L.out = off;                                      // [bufs][m_pad][tile_n] bf16 staging for C
+        off += out_bytes;
+    }
     L.bars = off;                                         // full[stages], empty[stages], then per-kernel barriers
     off += (uint32_t)(2 * stages + 12) * 8u;
-    L.tmem_slot = off;
+    L.tmem_slot = off;                                    // u32 TMEM address, then (at +8) the u32 ticket counter
     off += 16;
     L.bytes = off + 1024;                                 // slack to align the dynamic base
     return L;
@@ -271,6 +298,72 @@ __device__ __forceinline__ void record_error(const KernelParams &p, uint32_t bit
     atomicOr(p.status, bits);
 }
 
+// The owner's wait for its mailbox (relaxed, cluster scope).  If it runs out,
+// the error is recorded and the owner waits once more with the same bound
+// before going on: a peer that is only slow then finishes its st.async writes
+// into this CTA's shared memory before the CTA can exit (a write that lands
+// after the owner has exited would be undefined).  The second wait also ends,
+// so a peer that never writes (a dropped mailbox) costs two bounds, not a hang.
+__device__ __forceinline__ bool owner_wait_mailbox(const KernelParams &p, uint32_t bar, uint32_t parity)
+{
+    if (wait_bounded<true>(bar, parity, p.reduce_timeout_ns))
+        return true;
+    record_error(p, kErrReduce);
+    (void)wait_bounded<true>(bar, parity, p.reduce_timeout_ns);
+    return false;
+}
+
+// A peer's wait, before its first st.async, for the owner's "mailbox open"
+// arrival when the mailbox aliases the owner's ring (relaxed cluster-scope
+// observation, then the acquire fence restricted to shared::cluster, as for
+// the owner's mailbox wait).  Without aliasing the mailbox is always open.
+__device__ __forceinline__ bool peer_wait_mailbox_open(const KernelParams &p, bool alias, uint32_t bar_open)
+{
+    if (!alias)
+        return true;
+    const bool open = wait_bounded<true>(bar_open, 0, p.timeout_ns);
+    if (!open)
+        record_error(p, kErrMailboxOpen);
+    ptx::fence_acquire_shared_cluster();
+    return open;
+}
+
+// Stress probes of the TMEM release order.  An epilogue warp calls
+// probe_loads_done after its last tcgen05.wait::ld and before its release
+// arrival: the latest %globaltimer of the warp goes to probes[0] and lane 0
+// takes one ticket from the CTA's shared counter.  The MMA warp calls
+// probe_before_dealloc after its release waits, just before tcgen05.dealloc:
+// it stores %globaltimer in probes[1] and the tickets it can see in probes[2].
+// The tickets make the order exact rather than a comparison of two clock
+// reads: each ticket is taken before its warp's release arrival, and the MMA
+// warp reads the counter after observing the phase those arrivals complete,
+// so it must see all four when the protocol holds; a dealloc that could
+// precede an epilogue load would see fewer.
+__device__ __forceinline__ void probe_loads_done(const KernelParams &p, unsigned long long t, int lane,
+                                                 uint32_t ticket_addr)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (lane == 0) {
+        atomicMax(&p.probes[kProbeWords * blockIdx.x], t);
+        ptx::atomic_add_shared(ticket_addr, 1u);
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void probe_before_dealloc(const KernelParams &p, int lane, uint32_t ticket_addr)
+{
+    if (lane == 0) {
+        const unsigned long long tickets = ptx::ld_volatile_shared(ticket_addr);
+        const uint64_t t = ptx::globaltimer();
+        ptx::griddep_wait();                       // the probe buffer may be written by the previous kernel
+        p.probes[kProbeWords * blockIdx.x + 1] = t;
+        p.probes[kProbeWords * blockIdx.x + 2] = tickets;
+    }
+    __syncwarp();
+}
+
 // The owner's stores of one staged tile: rows m < M of [m_pad][tile_n] bf16
 // staging, columns below N.  16-byte stores when N % 8 == 0 (row m of the tile
 // is tile_n / 8 chunks; a partial last tile stores only the chunks below N),
@@ -304,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(M_PAD % (TILE_N == 128 ? 16 : 8) == 0 && M_PAD >= 8 && M_PAD <= 128,
                   "m_pad is the MMA N: a multiple of 8 (M = 64) or 16 (M = 128), at most 128");
     constexpr int kTileN = TILE_N;
-    static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
+    static_assert(SPLIT_K == 1 || SPLIT_K == 2 || SPLIT_K == 3 || SPLIT_K == 4 || SPLIT_K == 8, "split_k");
     constexpr uint32_t kAcc1 = M_PAD <= 16 ? 16u : (uint32_t)M_PAD;   // column of accumulator 1
     constexpr uint32_t kTmemCols = tmem_cols_for(kAcc1 + M_PAD);
     constexpr uint32_t kSlotBytes = kTileN * M_PAD * 4u;          // one rank's fp32 partial tile
@@ -312,18 +405,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int kbs = p.kb_per_stage;
-    const SmemLayout L = make_smem_layout(TILE_N, M_PAD, SPLIT_K, p.stages, kbs);
+    const bool alias = SPLIT_K > 1 && p.mbox_in_ring != 0;       // mailbox + staging in the drained ring
+    const SmemLayout L = make_smem_layout(TILE_N, M_PAD, SPLIT_K, p.stages, kbs, 1, alias);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int stages = p.stages;
     const uint32_t w_stage_bytes = (uint32_t)kbs * w_block_bytes(TILE_N);
     const uint32_t a_stage_bytes = (uint32_t)kbs * (M_PAD * 128u);
     const uint32_t stage_tx = w_stage_bytes + a_stage_bytes;
-    const int n_stages = p.kb_per_rank / kbs;                     // stage iterations of this rank
+    // This rank's stages of the K range: an even share when split_k divides
+    // the stage count, otherwise the first ranks take one stage fewer.
+    const uint32_t rank_ = SPLIT_K > 1 ? ptx::cluster_ctarank() : 0u;
+    const int s_begin = (int)(((long long)rank_ * p.stages_total) / SPLIT_K);
+    const int n_stages = (int)((((long long)rank_ + 1) * p.stages_total) / SPLIT_K) - s_begin;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = SPLIT_K > 1 ? ptx::cluster_ctarank() : 0u;
+    const uint32_t rank = rank_;
     const int n0 = (int)(blockIdx.x / SPLIT_K) * kTileN;
-    const int kb0 = (int)rank * p.kb_per_rank;
+    const int kb0 = s_begin * kbs;
 
     const uint32_t bar_full = sbase + L.bars;                      // + 8 * stage
     const uint32_t bar_empty = bar_full + 8u * stages;             // + 8 * stage
@@ -331,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_tmem_alloc = bar_acc + 8u;                  // two phases, 160 arrivals each
     const uint32_t bar_reduce = bar_acc + 16u;                     // owner's mailbox barrier
     const uint32_t bar_reduce2 = bar_acc + 24u;                    // second half of the mailbox (two-phase)
+    const uint32_t bar_open = bar_acc + 32u;                       // peers: the owner's ring is drained (alias)
     // m_pad 64 splits each slot's float4 columns into two halves with a
     // barrier each, so the owner reduces and stages the first half while the
     // second is still arriving (GB300, M64 N6144 K4096: 11.55 -> 11.31 us; at
@@ -349,6 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_tmem_alloc, kTmemBarArrivals);
         ptx::mbar_init(bar_reduce, 1);
         ptx::mbar_init(bar_reduce2, 1);
+        ptx::mbar_init(bar_open, 1);                       // one remote arrival from the owner
+        *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot + kTicketOffset) = 0u;
         if (SPLIT_K > 1 && rank == 0) {   // arm the mailbox: every peer sends one full partial tile
             if (kTwoPhase) {
                 ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 2);
@@ -415,6 +516,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < pre; ++i)
                 ptx::tma_load_3d(sbase + L.a + (uint32_t)i * a_stage_bytes, &tmap_a, 0, 0, kb0 + i * kbs,
                                  bar_full + 8u * i, pol_a);
+            // L2 prefetch: keep the W stages up to l2_prefetch_stages beyond the
+            // newest ring load requested into L2, so that more of W is in
+            // flight than the ring's shared memory holds.
+            const int l2pf = (int)p.l2_prefetch_stages;
+            int next_pf = pre;
+            while (next_pf < n_stages && next_pf < pre + l2pf) {
+                ptx::tma_prefetch_3d(&tmap_w, 0, n0, kb0 + next_pf * kbs);
+                ++next_pf;
+            }
             int issued = pre;
             for (int i = pre; i < n_stages; ++i) {
                 const int s = i % stages;
@@ -430,6 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(sbase + L.a + (uint32_t)s * a_stage_bytes, &tmap_a, 0, 0, kz, bar_full + 8u * s,
                                  pol_a);
                 ++issued;
+                while (next_pf < n_stages && next_pf <= i + l2pf) {
+                    ptx::tma_prefetch_3d(&tmap_w, 0, n0, kb0 + next_pf * kbs);
+                    ++next_pf;
+                }
             }
             ptx::griddep_launch_dependents();
             // No copy may still be landing in this CTA's shared memory when it exits:
@@ -491,12 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bounded<false>(bar_acc, 0, kDrainTimeoutNs))
             record_error(p, kErrMmaAccDrain);
         ptx::tcgen05_fence_after_thread_sync();
-        if (p.probes != nullptr && lane == 0) {
-            const uint64_t t = ptx::globaltimer();
-            ptx::griddep_wait();                   // the probe buffer may be written by the previous kernel
-            p.probes[2 * blockIdx.x + 1] = t;
-        }
-        __syncwarp();
+        if (p.probes != nullptr)
+            probe_before_dealloc(p, lane, tmem_slot + kTicketOffset);
         ptx::tmem_dealloc(tmem_d, kTmemCols);
     } else if (warp == kMmaWarp2) {
         // ------------------------------------------------------------ second MMA issuer
@@ -549,6 +659,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
         }
         ptx::tcgen05_fence_after_thread_sync();
+        if (alias && rank == 0 && etid == 0 && ok) {
+            // Every MMA of this CTA has completed (bar_acc), so no copy lands in
+            // and no MMA reads the ring any more: open the mailbox that aliases
+            // it to every peer (a release arrival on each peer's bar_open).
+            ptx::fence_proxy_async_shared();
+#pragma unroll 1
+            for (int r = 1; r < SPLIT_K; ++r)
+                ptx::mbar_arrive_remote_release_cluster(ptx::mapa_shared(bar_open, (uint32_t)r));
+        }
         ok = __all_sync(0xffffffffu, ok);          // tcgen05.ld is warp-collective
 
         if constexpr (M_PAD <= 64) {
@@ -565,14 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < M_PAD; ++i)
                     acc[i] = 0.0f;
             }
-            if (p.probes != nullptr) {
-                unsigned long long t = ptx::globaltimer();
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
-                if (lane == 0)
-                    atomicMax(&p.probes[2 * blockIdx.x], t);
-            }
+            if (p.probes != nullptr)
+                probe_loads_done(p, ptx::globaltimer(), lane, tmem_slot + kTicketOffset);
             ptx::tcgen05_fence_before_thread_sync();
             ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
 
@@ -580,7 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
             if (SPLIT_K > 1 && rank != 0) {
                 // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
-                if (ok && valid && !p.drop_mailbox) {
+                const bool open = peer_wait_mailbox_open(p, alias, bar_open);
+                if (ok && open && valid && !p.drop_mailbox) {
                     const uint32_t dst = ptx::mapa_shared(
                         sbase + L.mailbox + (rank - 1u) * kSlotBytes + 16u * (uint32_t)row, 0);
                     const uint32_t rbar = ptx::mapa_shared(bar_reduce, 0);
@@ -601,10 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     bool okh = ok;
-                    if (!wait_bounded<true>(h == 0 ? bar_reduce : bar_reduce2, 0, p.reduce_timeout_ns)) {
-                        record_error(p, kErrReduce);
+                    if (!owner_wait_mailbox(p, h == 0 ? bar_reduce : bar_reduce2, 0))
                         okh = false;
-                    }
                     ptx::fence_acquire_shared_cluster();
                     if (valid) {
                         if (okh) {
@@ -640,10 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (SPLIT_K > 1) {
                     // Owner: relaxed cluster-scope observation of the mailbox phase,
                     // then one acquire fence restricted to shared::cluster memory.
-                    if (!wait_bounded<true>(bar_reduce, 0, p.reduce_timeout_ns)) {
-                        record_error(p, kErrReduce);
+                    if (!owner_wait_mailbox(p, bar_reduce, 0))
                         ok = false;
-                    }
                     ptx::fence_acquire_shared_cluster();
                     if (valid && ok) {
                         const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
@@ -711,17 +821,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
             const bool owner = !(SPLIT_K > 1 && rank != 0);
             if (owner && SPLIT_K > 1) {
-                if (!wait_bounded<true>(bar_reduce, 0, p.reduce_timeout_ns)) {
-                    record_error(p, kErrReduce);
+                if (!owner_wait_mailbox(p, bar_reduce, 0))
                     ok = false;
-                }
                 ptx::fence_acquire_shared_cluster();
             }
             ok = __all_sync(0xffffffffu, ok);
             __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
             const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
             uint32_t dst = 0, rbar = 0;
+            bool open = true;
             if (!owner) {
+                open = peer_wait_mailbox_open(p, alias, bar_open);
                 dst = ptx::mapa_shared(sbase + L.mailbox + (rank - 1u) * kSlotBytes + 16u * (uint32_t)row, 0);
                 rbar = ptx::mapa_shared(bar_reduce, 0);
             }
@@ -741,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc[i] = 0.0f;
                 }
                 if (!owner) {
-                    if (ok && valid && !p.drop_mailbox) {
+                    if (ok && open && valid && !p.drop_mailbox) {
 #pragma unroll
                         for (int i = 0; i < kCh / 4; ++i)          // slot layout [m_pad / 4][tile_n] float4
                             ptx::st_async_v4(dst + 16u * kTileN * (uint32_t)(c0 / 4 + i), rbar, acc[4 * i],
@@ -773,14 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.probes != nullptr) {
-                unsigned long long t = ptx::globaltimer();
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
-                if (lane == 0)
-                    atomicMax(&p.probes[2 * blockIdx.x], t);
-            }
+            if (p.probes != nullptr)
+                probe_loads_done(p, ptx::globaltimer(), lane, tmem_slot + kTicketOffset);
             ptx::tcgen05_fence_before_thread_sync();
             ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: this thread's TMEM reads are done
             if (owner) {

@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreadsPersistent, 1)
             ptx::mbar_init(bar_mbox_free + 8u * b, 1);
         }
         ptx::mbar_init(bar_tmem_alloc, kTmemBarArrivals);
+        *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot + kTicketOffset) = 0u;
         if (SPLIT_K > 1 && rank == 0)              // arm both mailbox buffers for the first two tiles
             for (int b = 0; b < 2 && b < my_tiles; ++b)
                 ptx::mbar_arrive_expect_tx(bar_reduce + 8u * b, kSetBytes);
@@ -206,12 +207,8 @@ __global__ void __launch_bounds__(kThreadsPersistent, 1)
                 record_error(p, kErrMmaAccDrain);
         }
         ptx::tcgen05_fence_after_thread_sync();
-        if (p.probes != nullptr && lane == 0) {
-            const uint64_t t = ptx::globaltimer();
-            ptx::griddep_wait();
-            p.probes[2 * blockIdx.x + 1] = t;
-        }
-        __syncwarp();
+        if (p.probes != nullptr)
+            probe_before_dealloc(p, lane, tmem_slot + kTicketOffset);
         ptx::tmem_dealloc(tmem_d, kTmemCols);
     } else {
         // ------------------------------------------------------------ epilogue warps
@@ -274,10 +271,8 @@ __global__ void __launch_bounds__(kThreadsPersistent, 1)
             } else {
                 bool red_ok = true;
                 if (SPLIT_K > 1) {
-                    if (!wait_bounded<true>(bar_reduce + 8u * b, u & 1u, p.reduce_timeout_ns)) {
-                        record_error(p, kErrReduce);
+                    if (!owner_wait_mailbox(p, bar_reduce + 8u * b, u & 1u))
                         red_ok = false;
-                    }
                     ptx::fence_acquire_shared_cluster();
                     if (valid && red_ok) {
                         const float *box = reinterpret_cast<const float *>(smem + L.mailbox + (uint32_t)b * kSetBytes);
@@ -339,13 +334,8 @@ __global__ void __launch_bounds__(kThreadsPersistent, 1)
         }
         if (p.timeline != nullptr && etid == 0)
             p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
-        if (p.probes != nullptr) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                t_ld = max(t_ld, __shfl_xor_sync(0xffffffffu, t_ld, o));
-            if (lane == 0)
-                atomicMax(&p.probes[2 * blockIdx.x], t_ld);
-        }
+        if (p.probes != nullptr)
+            probe_loads_done(p, t_ld, lane, tmem_slot + kTicketOffset);
         ptx::tcgen05_fence_before_thread_sync();
         ptx::mbar_arrive(bar_tmem_alloc);          // second arrival: every TMEM read of this thread is done
     }

@@ -211,6 +211,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// L2 prefetch of the same 3-D box (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int32_t x, int32_t y, int32_t z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 // Allocation: executed by one whole warp; writes the TMEM base address to
 // shared memory at `dst`.
@@ -287,6 +296,20 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t
 __device__ __forceinline__ void tmem_wait_st()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Relaxed atomic add on a 32-bit shared-memory word (CTA scope).
+__device__ __forceinline__ void atomic_add_shared(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.relaxed.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Volatile load of a 32-bit shared-memory word.
+__device__ __forceinline__ uint32_t ld_volatile_shared(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.volatile.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id `id` (1..15).

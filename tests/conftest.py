@@ -26,3 +26,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the per-call parity records (outputs beyond 1 ulp, exemptions) when LOWM_PARITY_LOG names a file."""
+    try:
+        import helpers
+    except Exception:  # pragma: no cover
+        return
+    helpers.write_parity_log()

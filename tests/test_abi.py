@@ -59,17 +59,36 @@ def test_shipped_tactic_is_reproduced(L, monkeypatch):
 
 
 def test_default_tactic_for_the_headline_workload(L):
+    # GB300 with the one-stage L2 prefetch: 128-column tiles, one CTA per SM
+    # on 96 SMs (9.43 us) beat the 64-column tiles on 192 CTAs (10.14 us).
     st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
     assert st == lowm.LOWM_OK
-    assert (t["tile_n"], t["m_pad"], t["split_k"], t["kb_per_stage"], t["stages"]) == (64, 8, 2, 4, 3)
-    assert t["num_clusters"] == 96 and t["ctas"] == 192 and t["persistent"] == 0 and t["smem_bytes"] <= 232448
+    assert (t["tile_n"], t["m_pad"], t["split_k"], t["kb_per_stage"], t["stages"]) == (128, 16, 2, 4, 2)
+    assert t["num_clusters"] == 48 and t["ctas"] == 96 and t["persistent"] == 0 and t["smem_bytes"] <= 232448
+    assert t["l2_prefetch_stages"] == 1 and t["mbox_in_ring"] == 0
 
 
-@pytest.mark.parametrize("M,tile", [(4, 64), (8, 64), (9, 128), (16, 128), (17, 64), (32, 64), (33, 128), (64, 128),
-                                    (65, 64), (128, 64)])
-def test_tile_width_follows_m_pad(L, M, tile):
-    st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 2)
+@pytest.mark.parametrize("M,N,K,sk,tile", [
+    # 128 columns where the 64-column grid overflows the SMs and the 128-column grid fits with a short stream
+    (4, 6144, 4096, 2, 128), (16, 6144, 4096, 2, 128), (32, 6144, 4096, 2, 128), (64, 6144, 4096, 2, 128),
+    (128, 6144, 4096, 2, 128),
+    (4, 2304, 12288, 4, 64),      # the 64-column grid (144 CTAs) already fits
+    (4, 49152, 4096, 2, 64),      # both widths overflow the SMs
+    (16, 6144, 32768, 4, 64),     # both overflow
+    (16, 6144, 32768, 2, 64),     # fits, but 4 MiB of W per 128-column CTA
+    (4, 6152, 4096, 2, 64)])      # N not a multiple of 128
+def test_tile_width_rule(L, M, N, K, sk, tile):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
     assert st == lowm.LOWM_OK and t["tile_n"] == tile
+
+
+@pytest.mark.parametrize("M,N,K,sk,tile", [
+    (1, 6144, 4096, 2, 128), (64, 6144, 4096, 2, 128), (128, 6144, 4096, 2, 128),   # short GEMMs: 96 CTAs
+    (4, 2304, 12288, 4, 64),      # fills 90 % of the SMs with 64-column tiles (split 8 measured slower)
+    (4, 49152, 4096, 1, 64), (16, 6144, 32768, 2, 64)])
+def test_auto_split_is_the_measured_best(L, M, N, K, sk, tile):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, 0)
+    assert st == lowm.LOWM_OK and (t["split_k"], t["tile_n"]) == (sk, tile)
 
 
 @pytest.mark.parametrize("M,N,K,sk", [(4, 2304, 12288, 4), (4, 49152, 4096, 2), (16, 6144, 32768, 4),
@@ -144,7 +163,7 @@ def test_any_n_is_tiled_with_a_partial_last_tile(L, M, N, K, sk):
 
 @pytest.mark.parametrize("M,N,K,sk,wpf", [
     # one W stage ahead of the PDL wait for three-stage 64-column rings, the whole ring otherwise (GB300 sweep)
-    (4, 6144, 4096, 2, 1), (1, 6144, 4096, 2, 1), (8, 6144, 4096, 2, 1), (4, 2304, 12288, 4, 2), (4, 49152, 4096, 2, 2),
+    (4, 6152, 4096, 2, 1), (4, 6144, 4096, 2, 2), (8, 6144, 4096, 2, 2), (4, 2304, 12288, 4, 2), (4, 49152, 4096, 2, 2),
     (16, 6144, 32768, 4, 2), (64, 6144, 4096, 2, 3), (32, 6144, 4096, 2, 2)])
 def test_two_mma_issuers_and_prefetch_depth(L, M, N, K, sk, wpf):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
@@ -172,10 +191,11 @@ def test_persistent_schedule_has_one_issuer(L, monkeypatch):
 @pytest.mark.parametrize("M", [65, 96, 127, 128])
 def test_m_up_to_128_pads_to_128(L, M, monkeypatch):
     monkeypatch.setenv("LOWM_PERSISTENT", "1")      # no persistent m_pad 128 instance: ignored
-    for sk in (1, 2, 4):
+    for sk in (1, 2, 3, 4):
         st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, sk)
         assert st == lowm.LOWM_OK and t["m_pad"] == 128 and t["persistent"] == 0 and t["mma_issuers"] == 2
         assert t["smem_bytes"] <= 232448
+        assert t["mbox_in_ring"] == (1 if sk > 1 else 0)       # the 32-64 KiB slots share the drained ring
     st, t = lowm.lowm_gemm_query_tactic(M, 64, 8192, 0)   # one tile: auto split stops where the mailbox fits
     assert st == lowm.LOWM_OK and t["split_k"] == 4
 
@@ -201,7 +221,9 @@ def test_auto_split_k_keeps_the_k_loop_non_empty(L):
     (128, 64, 1024, 8, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),   # m_pad 128: the split-8 mailbox does not fit
     (4, 64, 96, 1, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # K not a multiple of 64
     (4, 64, 64, 2, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),      # empty K loop on one rank
-    (4, 64, 128, 3, lowm.LOWM_ERR_INVALID_ARGUMENT),      # split_k not a power of two
+    (4, 64, 128, 3, lowm.LOWM_ERR_UNSUPPORTED_SHAPE),     # 2 K blocks for 3 ranks: an empty share
+    (4, 64, 128, 5, lowm.LOWM_ERR_INVALID_ARGUMENT),      # split_k outside {0, 1, 2, 3, 4, 8}
+    (4, 64, 64 * 5, 6, lowm.LOWM_ERR_INVALID_ARGUMENT),
     (4, 64, 1024, 16, lowm.LOWM_ERR_INVALID_ARGUMENT),
     (4, -64, 64, 1, lowm.LOWM_ERR_INVALID_ARGUMENT),
 ])
@@ -277,8 +299,34 @@ def test_the_header_is_c99_and_links_against_the_library(L, tmp_path):
 
 @pytest.mark.parametrize("M", [96, 128])
 def test_m_pad_128_tactic_is_the_measured_best(L, M):
-    # GB300 sweep at N6144 K4096: split_k 1, 64-column tiles, 4 x 2 ring
-    # (15.8 us) beat every split-2 and 128-column choice (19.8-53 us).
+    # GB300 sweep at N6144 K4096 with the L2 prefetch: 128-column tiles,
+    # split_k 2, the mailbox in the drained ring, 2 x 3 ring: 14.1 us, against
+    # 15.8 us for split_k 1 on 64-column tiles and 15.8-18.2 us for other rings.
     st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 0)
     assert st == lowm.LOWM_OK
-    assert (t["tile_n"], t["split_k"], t["kb_per_stage"], t["stages"], t["ctas"]) == (64, 1, 4, 2, 96)
+    assert (t["tile_n"], t["split_k"], t["kb_per_stage"], t["stages"], t["ctas"], t["mbox_in_ring"]) == \
+        (128, 2, 2, 3, 96, 1)
+
+
+@pytest.mark.parametrize("K,sk", [(64 * 3, 2), (64 * 7, 3), (4096, 3), (64 * 50, 3), (64 * 9, 4)])
+def test_uneven_k_shares_are_accepted(L, K, sk):
+    # K is cut into whole stages; ranks whose share would be uneven take one
+    # stage fewer than the last ones, and every rank keeps at least one stage.
+    st, t = lowm.lowm_gemm_query_tactic(4, 640, K, sk)
+    assert st == lowm.LOWM_OK and t["split_k"] == sk
+    total = K // 64 // t["kb_per_stage"]
+    assert (K // 64) % t["kb_per_stage"] == 0 and total >= sk
+    shares = [(r + 1) * total // sk - r * total // sk for r in range(sk)]
+    assert min(shares) >= 1 and max(shares) - min(shares) <= 1 and sum(shares) == total
+
+
+def test_split3_defaults_to_the_mailbox_in_the_ring(L, monkeypatch):
+    st, t = lowm.lowm_gemm_query_tactic(64, 6144, 4096, 3)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0
+    monkeypatch.setenv("LOWM_MBOX_IN_RING", "0")
+    st, t = lowm.lowm_gemm_query_tactic(4, 640, 64 * 9, 3)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0
+    st, t = lowm.lowm_gemm_query_tactic(4, 640, 64 * 9, 1)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0          # no mailbox at split_k 1

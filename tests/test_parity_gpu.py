@@ -21,7 +21,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_parity, f32_bound
+from helpers import assert_parity
 from split_bf16_gemm_swap_gb300 import build, inputs, lowm
 
 pytestmark = pytest.mark.gpu
@@ -62,8 +62,7 @@ def check(A, W, split_k=0, exact=False):
         assert bad.size == 0, "first mismatches (m, n): %s" % bad[:8].tolist()
         assert np.array_equal(F, S)
         return C
-    bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
-    assert_parity(C, F, Cref, S, bound)
+    assert_parity(C, F, Cref, S, A, W, label="M%d N%d K%d split_k %d" % (M, W.shape[0], K, split_k))
     return C
 
 
@@ -118,8 +117,7 @@ def test_rows_beyond_M_are_not_written():
     sync_ok()
     assert torch.all(big[M:] == 7.0)
     Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
-    bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
-    assert_parity(inputs.bits(big[:M].cpu()), F.cpu().numpy().astype(np.float64), Cref, S, bound)
+    assert_parity(inputs.bits(big[:M].cpu()), F.cpu().numpy().astype(np.float64), Cref, S, A, W)
 
 
 # ---------------------------------------------------------------- the five workloads at full size
@@ -189,8 +187,7 @@ def test_pdl_chain_reads_the_previous_output():
     for i, w in enumerate(Ws):
         a = Cs[i].cpu()
         ref, S = oracle.gemm_bf16_f64(inputs.bits(a), inputs.bits(w))
-        bound = f32_bound(D, a.to(torch.float64).numpy(), w.to(torch.float64).numpy())
-        assert_parity(inputs.bits(Cs[i + 1].cpu()), Fs[i].cpu().numpy().astype(np.float64), ref, S, bound)
+        assert_parity(inputs.bits(Cs[i + 1].cpu()), Fs[i].cpu().numpy().astype(np.float64), ref, S, a, w)
 
 
 def test_host_buffer_entry_point_matches_device_path():
@@ -475,8 +472,7 @@ def test_n_tail_writes_nothing_past_n(N):
     sync_ok()
     assert torch.all(flat[M * N:] == 7.0)
     Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
-    bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
-    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, bound)
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, A, W)
 
 
 @pytest.mark.parametrize("tile", ["64", "128"])
@@ -584,8 +580,7 @@ def test_python_gemm_wrapper_allocates_and_raises():
     assert lowm.lowm_gemm_bf16_debug(A.to(DEV), W.to(DEV), Cd, M, N, K, 2, None, c_f32=F) == lowm.LOWM_OK
     sync_ok()
     assert torch.equal(C.view(torch.int16), Cd.view(torch.int16))       # the wrapper runs the same kernel
-    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S,
-                  f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy()))
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, A, W)
     C2 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
     assert lowm.gemm(A.to(DEV), W.to(DEV), C2, split_k=2) is C2
     sync_ok()
@@ -631,5 +626,97 @@ def test_fuzz_shapes_and_tactics(case, monkeypatch):
     assert lowm.lowm_gemm_bf16_debug(Ad, Wd, C, M, N, K, sk, None, c_f32=F, flags=flags) == lowm.LOWM_OK
     sync_ok()
     Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
-    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S,
-                  f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy()))
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, A, W)
+
+
+# ---------------------------------------------------------------- split_k 3 (uneven K shares) and the ring-aliased mailbox
+SPLIT3 = [
+    # M, N, K, tile: stage counts that 3 does not divide (the first ranks take one stage fewer), every m_pad
+    (1, 192, 64 * 4, "64"), (4, 640, 64 * 7, "64"), (8, 256, 64 * 64, "64"), (13, 384, 64 * 10, "128"),
+    (16, 6144, 4096, "128"), (32, 320, 64 * 11, "64"), (48, 256, 64 * 5, "128"), (64, 6144, 4096, "128"),
+    (64, 192, 64 * 3, "64"), (100, 130, 64 * 8, "64"), (128, 6144, 4096, "128"), (128, 6144, 4096, "64"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,tile", SPLIT3)
+def test_split3_random(M, N, K, tile, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, 3)
+    assert st == lowm.LOWM_OK and t["split_k"] == 3 and t["mbox_in_ring"] == 1
+    A, W = inputs.make_problem(M, N, K, seed=1100 + M + N + K)
+    check(A, W, 3)
+
+
+@pytest.mark.parametrize("M,tile", [(4, "64"), (16, "128"), (64, "128"), (128, "64"), (128, "128")])
+def test_split3_integer_exact(M, tile, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    N, K = 1024, 64 * 50                               # 50 blocks: shares of 16/17 blocks or whole uneven stages
+    A, W = inputs.make_problem(M, N, K, seed=19, kind="int")
+    C = check(A, W, 3, exact=True)
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(C, np.broadcast_to(inputs.bits(col[None, :]), C.shape))
+
+
+@pytest.mark.parametrize("kbs", ["1", "2", "4"])
+@pytest.mark.parametrize("tile", ["64", "128"])
+def test_split3_identity_weight_covers_every_k_step(kbs, tile, monkeypatch):
+    # W = I with N = K: every 16-wide K step of every rank's (uneven) share
+    # must land in the sum exactly once, whatever the stage size.
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    monkeypatch.setenv("LOWM_KB_PER_STAGE", kbs)
+    M, N, K = 16, 64 * 20, 64 * 20                     # 20 blocks: 5, 10 or 20 stages, none divisible by 3
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, 3)
+    assert st == lowm.LOWM_OK and t["kb_per_stage"] == int(kbs)
+    A = (torch.arange(M * K, dtype=torch.float32).reshape(M, K) % 241 - 120).to(torch.bfloat16)
+    W = torch.zeros((N, K), dtype=torch.bfloat16)
+    W[torch.arange(N), torch.arange(N)] = 1.0
+    C, F = run_gpu(A, W, 3)
+    assert np.array_equal(C, inputs.bits(A)), "an output column does not hold its own input column"
+    assert np.array_equal(F, A.to(torch.float64).numpy())
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 640, 64 * 6, 2), (64, 256, 2048, 2), (128, 384, 2048, 4),
+                                           (16, 6144, 4096, 2), (64, 1024, 64 * 3, 2)])
+def test_mailbox_in_ring_for_even_splits(M, N, K, split_k, monkeypatch):
+    # The aliased mailbox with split_k 2 and 4 (and an uneven split 2 of 3 blocks).
+    monkeypatch.setenv("LOWM_MBOX_IN_RING", "1")
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1
+    A, W = inputs.make_problem(M, N, K, seed=1200 + M + K)
+    check(A, W, split_k)
+
+
+def test_mailbox_next_to_ring_for_split3(monkeypatch):
+    monkeypatch.setenv("LOWM_MBOX_IN_RING", "0")
+    st, t = lowm.lowm_gemm_query_tactic(8, 640, 64 * 9, 3)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0
+    A, W = inputs.make_problem(8, 640, 64 * 9, seed=1300)
+    check(A, W, 3)
+
+
+@pytest.mark.parametrize("M,tile", [(4, "64"), (64, "128"), (128, "128")])
+def test_split3_dropped_mailbox_times_out(M, tile, monkeypatch):
+    # The peers skip their publication into the aliased mailbox: the owner's
+    # bounded waits run out, report the mailbox bit, and the context survives.
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    N, K = 256, 64 * 12
+    A, W = inputs.make_problem(M, N, K, seed=6)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    st = lowm.lowm_gemm_bf16_debug(A.to(DEV), W.to(DEV), C, M, N, K, 3, None, drop_mailbox=1,
+                                   reduce_timeout_ns=20_000_000)
+    assert st == lowm.LOWM_OK
+    st, detail = lowm.lowm_gemm_sync_status()
+    assert st == lowm.LOWM_ERR_TIMEOUT and detail == (1 << 8), (st, hex(detail))
+    check(A, W, 3)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 6144, 4096), (128, 6144, 4096)])
+def test_split3_twenty_launches_are_bitwise_identical(M, N, K):
+    A, W = inputs.make_problem(M, N, K, seed=34)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    outs = torch.empty((20, M, N), dtype=torch.bfloat16, device=DEV)
+    for i in range(20):
+        assert lowm.lowm_gemm_bf16(Ad, Wd, outs[i], M, N, K, 3, None) == lowm.LOWM_OK
+    sync_ok()
+    o = outs.view(torch.int16)
+    assert bool((o == o[0:1]).all())

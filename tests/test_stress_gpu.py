@@ -11,8 +11,10 @@ tcgen05.dealloc.  20 launches per configuration.
 
 Pass criteria: every stressed output is bitwise identical to the unstressed
 output (which is itself checked against the oracle / the closed form), no
-kernel wait times out, and in every CTA the dealloc timestamp is not earlier
-than the latest epilogue load.
+kernel wait times out, and in every CTA the MMA warp saw all four epilogue
+warps' ordering tickets just before tcgen05.dealloc (each ticket is taken
+after that warp's last tcgen05.wait::ld), with the dealloc timestamp not
+earlier than the latest epilogue load as a second, clock-based check.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_parity, f32_bound
+from helpers import assert_parity
 from split_bf16_gemm_swap_gb300 import build, inputs, lowm
 
 pytestmark = pytest.mark.gpu
@@ -43,7 +45,7 @@ def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0
     ctas = t["ctas"]
     s_gemm = torch.cuda.Stream()
     s_hog = torch.cuda.Stream()
-    probes = torch.zeros((LAUNCHES, ctas, 2), dtype=torch.int64, device=DEV)
+    probes = torch.zeros((LAUNCHES, ctas, 3), dtype=torch.int64, device=DEV)
     outs = torch.empty((LAUNCHES, M, N), dtype=torch.bfloat16, device=DEV)
     torch.cuda.synchronize()
     for i in range(LAUNCHES):
@@ -58,9 +60,15 @@ def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0
     return outs, probes.cpu().numpy()
 
 
+EPILOGUE_WARPS = 4
+
+
 def check_probes(p):
-    t_ld, t_dealloc = p[..., 0], p[..., 1]
+    t_ld, t_dealloc, tickets = p[..., 0], p[..., 1], p[..., 2]
     assert np.all(t_ld > 0) and np.all(t_dealloc > 0), "a CTA did not record both probes"
+    short = int(np.sum(tickets != EPILOGUE_WARPS))
+    assert short == 0, "%d of %d CTAs freed TMEM without all %d epilogue warps' tickets (seen: %s)" % (
+        short, tickets.size, EPILOGUE_WARPS, sorted(set(tickets.ravel().tolist())))
     early = int(np.sum(t_dealloc < t_ld))
     assert early == 0, "%d of %d CTAs freed TMEM before the epilogue's last load" % (early, t_ld.size)
 
@@ -73,6 +81,9 @@ CONFIGS = [
     (4, 49152, 4096, 2, "randn"),
     (64, 6144, 4096, 2, "randn"),          # 128-column tiles (MMA M = 128)
     (128, 6144, 4096, 2, "randn"),         # m_pad 128: chunked epilogue, release after the last chunk
+    (64, 6144, 4096, 3, "randn"),          # split_k 3: uneven K shares, mailbox in the drained ring
+    (128, 6144, 4096, 3, "randn"),
+    (16, 6144, 32768, 3, "int"),
 ]
 
 
@@ -90,8 +101,7 @@ def test_stalled_epilogue_with_tmem_hog(M, N, K, split_k, kind):
         assert np.array_equal(ref_bits, np.broadcast_to(inputs.bits(col[None, :]), ref_bits.shape))
     else:
         Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
-        bound = f32_bound(K, A.to(torch.float64).numpy(), W.to(torch.float64).numpy())
-        assert_parity(ref_bits, F.cpu().numpy().astype(np.float64), Cref, S, bound)
+        assert_parity(ref_bits, F.cpu().numpy().astype(np.float64), Cref, S, A, W)
     for stall_ns in (5_000, 10_000, 100_000):
         outs, probes = stressed(Ad, Wd, M, N, K, split_k, stall_ns)
         o = outs.view(torch.int16)
