@@ -430,6 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_reduce = bar_acc + 16u;                     // owner's mailbox barrier
     const uint32_t bar_reduce2 = bar_acc + 24u;                    // second half of the mailbox (two-phase)
     const uint32_t bar_open = bar_acc + 32u;                       // peers: the owner's ring is drained (alias)
+    // m_pad 128: one mailbox barrier per 32-column chunk (bar_reduce,
+    // bar_reduce2, bar_reduce3, bar_reduce4), so the owner reduces chunk c
+    // while the later chunks are still arriving.
+    const uint32_t bar_reduce3 = bar_acc + 40u;
+    const uint32_t bar_reduce4 = bar_acc + 48u;
     // m_pad 64 splits each slot's float4 columns into two halves with a
     // barrier each, so the owner reduces and stages the first half while the
     // second is still arriving (GB300, M64 N6144 K4096: 11.55 -> 11.31 us; at
@@ -449,9 +454,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_reduce, 1);
         ptx::mbar_init(bar_reduce2, 1);
         ptx::mbar_init(bar_open, 1);                       // one remote arrival from the owner
+        ptx::mbar_init(bar_reduce3, 1);
+        ptx::mbar_init(bar_reduce4, 1);
         *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot + kTicketOffset) = 0u;
         if (SPLIT_K > 1 && rank == 0) {   // arm the mailbox: every peer sends one full partial tile
-            if (kTwoPhase) {
+            if (M_PAD == 128) {
+                ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 4);
+                ptx::mbar_arrive_expect_tx(bar_reduce2, (SPLIT_K - 1) * kSlotBytes / 4);
+                ptx::mbar_arrive_expect_tx(bar_reduce3, (SPLIT_K - 1) * kSlotBytes / 4);
+                ptx::mbar_arrive_expect_tx(bar_reduce4, (SPLIT_K - 1) * kSlotBytes / 4);
+            } else if (kTwoPhase) {
                 ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 2);
                 ptx::mbar_arrive_expect_tx(bar_reduce2, (SPLIT_K - 1) * kSlotBytes / 2);
             } else {
@@ -519,6 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // L2 prefetch: keep the W stages up to l2_prefetch_stages beyond the
             // newest ring load requested into L2, so that more of W is in
             // flight than the ring's shared memory holds.
+            // (Requested before the dependency wait instead, they slowed the
+            // preceding kernel's tail: 9.53 -> 11.0 us at M4 N6144 K4096.)
             const int l2pf = (int)p.l2_prefetch_stages;
             int next_pf = pre;
             while (next_pf < n_stages && next_pf < pre + l2pf) {
@@ -812,31 +826,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             // m_pad 128: two 128-column accumulators do not fit in registers, so
-            // the epilogue works in 32-column chunks.  The owner waits for the
-            // whole mailbox first; every thread makes its second (TMEM-release)
-            // arrival only after its last chunk's tcgen05.wait::ld.
+            // the epilogue works in 32-column chunks.  Each chunk of the mailbox
+            // has its own barrier: a peer credits chunk c's barrier with its
+            // chunk-c stores, and the owner waits for chunk c only when it
+            // reduces it, while the later chunks are still arriving.  Every
+            // thread makes its second (TMEM-release) arrival only after its last
+            // chunk's tcgen05.wait::ld.
             constexpr int kCh = 32;
+            static_assert(M_PAD == 4 * kCh, "one mailbox barrier per 32-column chunk");
             const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
             int row;
             const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
             const bool owner = !(SPLIT_K > 1 && rank != 0);
-            if (owner && SPLIT_K > 1) {
-                if (!owner_wait_mailbox(p, bar_reduce, 0))
-                    ok = false;
-                ptx::fence_acquire_shared_cluster();
-            }
-            ok = __all_sync(0xffffffffu, ok);
             __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
             const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
-            uint32_t dst = 0, rbar = 0;
+            uint32_t dst = 0;
             bool open = true;
             if (!owner) {
                 open = peer_wait_mailbox_open(p, alias, bar_open);
                 dst = ptx::mapa_shared(sbase + L.mailbox + (rank - 1u) * kSlotBytes + 16u * (uint32_t)row, 0);
-                rbar = ptx::mapa_shared(bar_reduce, 0);
             }
 #pragma unroll 1
             for (int c0 = 0; c0 < M_PAD; c0 += kCh) {
+                const int c = c0 / kCh;
+                const uint32_t bar_c = c == 0 ? bar_reduce : c == 1 ? bar_reduce2 : c == 2 ? bar_reduce3 : bar_reduce4;
                 float acc[kCh];
                 if (ok) {
                     float acc1[kCh];
@@ -852,13 +865,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!owner) {
                     if (ok && open && valid && !p.drop_mailbox) {
+                        const uint32_t rbar = ptx::mapa_shared(bar_c, 0);
 #pragma unroll
                         for (int i = 0; i < kCh / 4; ++i)          // slot layout [m_pad / 4][tile_n] float4
                             ptx::st_async_v4(dst + 16u * kTileN * (uint32_t)(c0 / 4 + i), rbar, acc[4 * i],
                                              acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
                     }
-                } else if (valid) {
-                    if (SPLIT_K > 1 && ok) {
+                } else {
+                    bool okc = ok;
+                    if (SPLIT_K > 1) {
+                        // Relaxed cluster-scope observation of chunk c, then the
+                        // acquire fence restricted to shared::cluster.
+                        if (!owner_wait_mailbox(p, bar_c, 0))
+                            okc = false;
+                        ptx::fence_acquire_shared_cluster();
+                    }
+                    if (valid && SPLIT_K > 1 && okc) {
 #pragma unroll 1
                         for (int r = 1; r < SPLIT_K; ++r) {    // fixed rank order
                             const float4 *src = box + (r - 1) * (kSlotBytes / 16) + (c0 / 4) * kTileN + row;
@@ -872,14 +894,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-#pragma unroll
-                    for (int i = 0; i < kCh; ++i)
-                        stage_out[(c0 + i) * kTileN + row] = __float2bfloat16_rn(acc[i]);
-                    if (p.c_f32 != nullptr) {
+                    if (valid) {
 #pragma unroll
                         for (int i = 0; i < kCh; ++i)
-                            if (c0 + i < p.M && n0 + row < p.N)
-                                p.c_f32[(size_t)(c0 + i) * p.N + n0 + row] = acc[i];
+                            stage_out[(c0 + i) * kTileN + row] = __float2bfloat16_rn(acc[i]);
+                        if (p.c_f32 != nullptr) {
+#pragma unroll
+                            for (int i = 0; i < kCh; ++i)
+                                if (c0 + i < p.M && n0 + row < p.N)
+                                    p.c_f32[(size_t)(c0 + i) * p.N + n0 + row] = acc[i];
+                        }
                     }
                 }
             }
