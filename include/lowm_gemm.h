@@ -58,9 +58,13 @@ typedef enum {
 /*
  * A tactic: how one GEMM is tiled and launched.
  *   tile_n       output columns per CTA; the MMA's M dimension (swap-AB: N is
- *                mapped onto the tensor core's M, the tiny M onto its N)
- *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64 or 128);
- *                rows M..m_pad-1 are zero-filled by the TMA unit and never stored
+ *                mapped onto the tensor core's M, the tiny M onto its N): 128
+ *                when N % 128 == 0, the 64-column grid would not fit the GPU
+ *                at one CTA per SM while the 128-column grid does, and each
+ *                128-column CTA streams at most 1 MiB of W; else 64
+ *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64 or 128;
+ *                at least 16 for 128-column tiles); rows M..m_pad-1 are
+ *                zero-filled by the TMA unit and never stored
  *   split_k      CTAs per cluster along K (1, 2, 3, 4 or 8).  K is cut into
  *                stages of kb_per_stage 64-wide blocks and rank r takes
  *                stages [r*T/split_k, (r+1)*T/split_k) of the T in all, so
@@ -75,9 +79,9 @@ typedef enum {
  *   pdl          1 when launched with programmatic dependent launch
  *   persistent   1: each cluster walks tiles c, c + num_clusters, ... with a
  *                continuous TMA stream and double-buffered accumulator,
- *                mailbox and output staging (chosen when there are more tiles
- *                than clusters that fit on the GPU at once; every cluster then
- *                gets the same number of tiles, tiles_per_cluster)
+ *                mailbox and output staging (opt-in with the environment
+ *                variable LOWM_PERSISTENT=1, even K splits only; every cluster
+ *                then gets the same number of tiles, tiles_per_cluster)
  *   tiles_per_cluster  ceil(tiles / num_clusters)
  *   kb_per_stage 64-wide K blocks per ring stage, fetched by one 3-D TMA
  *                copy of W and one of A (the largest of 8, 4, 2, 1 that
@@ -164,16 +168,26 @@ lowm_status_t lowm_gemm_bf16_ex(const void *A, const void *W, void *C,
 /*
  * Fill *out with the tactic lowm_gemm_bf16 would launch for these arguments
  * (host only; no device work).  Same argument rules and status codes as
- * lowm_gemm_bf16, minus the pointer checks.
+ * lowm_gemm_bf16, minus the pointer checks.  The PR page runs its kernel with
+ * a host-chosen tactic ("Fix two synchronization gaps ...", Hardware
+ * verification: the shipped (64, 8, 2, 10) tactic, 96 clusters / 192 CTAs at
+ * M4 N6144 K4096); it defines no query, and this one reports the table's
+ * choice (tile, padding, split, ring, grid, shared memory) for a shape.
  */
 lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tactic_t *out);
 
-/* A static, human-readable name for a status code (never NULL). */
+/* A static, human-readable name for a status code (never NULL).  The pages'
+ * kernel reports no errors, so this helper of the boundary has no passage
+ * behind it. */
 const char *lowm_status_string(lowm_status_t status);
 
 /*
  * Synchronize `stream`, then read and clear the device status word that the
- * kernels set when a bounded wait gives up.  Returns LOWM_ERR_TIMEOUT if any
+ * kernels set when a bounded wait gives up.  The pages' kernel waits without
+ * a bound (the PR page's Description, item 1, notes that the missing phase-0
+ * wait does not hang); this library bounds every wait on another party (2 s)
+ * so that a lost arrival ends the kernel with a recorded error instead of a
+ * hung GPU, and this call is how the host learns of it.  Returns LOWM_ERR_TIMEOUT if any
  * kernel since the last call recorded one (the word's bits are written to
  * *detail when detail is non-NULL), LOWM_ERR_CUDA if synchronization failed,
  * else LOWM_OK.
