@@ -165,13 +165,17 @@ struct Ring {
     int kbs, stages;
 };
 
-constexpr int kMaxRingBytes = 160 * 1024;
+constexpr int kMaxRingBytes = 160 * 1024;     // W bytes per ring when several CTAs share an SM
 
 Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int sms, int bufs, bool alias = false)
 {
     const int per_sm_one_wave = (ctas + std::max(1, sms) - 1) / std::max(1, sms);
     const int per_sm = per_sm_one_wave <= 4 ? std::max(1, per_sm_one_wave) : (split_k == 1 ? 3 : 5);
     const int budget = std::min(kMaxSmemPerCta, kSmemPerSm / per_sm - kSmemReservedPerCta);
+    // One CTA per SM: the ring may take all of the SM's shared memory (a
+    // 128-column M4 N6144 K4096 CTA with a 4 x 3 ring, 192 KiB of W, measured
+    // 8.90 us against 9.57 us with the 4 x 2 ring the 160 KiB cap allowed).
+    const int cap = per_sm == 1 ? kMaxSmemPerCta : kMaxRingBytes;
     int force_kbs = env_int("LOWM_KB_PER_STAGE", 0);
     if (force_kbs != 1 && force_kbs != 2 && force_kbs != 4 && force_kbs != 8)
         force_kbs = 0;
@@ -185,7 +189,7 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int
     } else {
         for (int b = 8; b >= 1; b /= 2)
             if (kbs_tiles_k(b, kb_total, split_k) && footprint(tile_n, m_pad, split_k, 2, b, bufs, alias) <= budget &&
-                ring_bytes(b, 2) <= kMaxRingBytes) {
+                ring_bytes(b, 2) <= cap) {
                 kbs = b;
                 break;
             }
@@ -195,7 +199,7 @@ Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int
         st = force_st;
     } else {
         while (st < 32 && footprint(tile_n, m_pad, split_k, st + 1, kbs, bufs, alias) <= budget &&
-               ring_bytes(kbs, st + 1) <= kMaxRingBytes)
+               ring_bytes(kbs, st + 1) <= cap)
             ++st;
     }
     return Ring{kbs, st};
@@ -245,15 +249,25 @@ int m_pad_for(int M, int tile_n)
 // The split-K mailbox shares the drained ring (see make_smem_layout) for
 // split_k 3 and for m_pad 128, whose 32-64 KiB slots would otherwise take the
 // ring's room (M128 N6144 K4096 split_k 2 on 128-column tiles: 14.4 us
-// against 16.4 us with the mailbox next to the ring).  LOWM_MBOX_IN_RING =
-// 0 / 1 overrides (tuning).
-bool choose_alias(int m_pad, int split_k)
+// against 16.4 us with the mailbox next to the ring), and otherwise whenever
+// sharing lets the ring hold more W (make_tactic compares both layouts; M4
+// N6144 K4096: a 4 x 3 ring, 8.90 us, against 4 x 2, 9.57 us; M64 4 x 2
+// against 2 x 3, 10.66 against 10.97 us).  LOWM_MBOX_IN_RING = 0 / 1
+// overrides (tuning).  Returns 1 / 0 when the choice is fixed, -1 when the
+// ring sizes decide.
+int forced_alias(int m_pad, int split_k)
 {
-    bool alias = split_k == 3 || (m_pad == 128 && split_k > 1);
+    if (split_k == 1)
+        return 0;
     const int force = env_int("LOWM_MBOX_IN_RING", -1);
     if (force == 0 || force == 1)
-        alias = force == 1;
-    return alias && split_k > 1;
+        return force;
+    return (split_k == 3 || m_pad == 128) ? 1 : -1;
+}
+
+bool choose_alias(int m_pad, int split_k)
+{
+    return forced_alias(m_pad, split_k) == 1;
 }
 
 KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent);
@@ -418,25 +432,46 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1); it splits K evenly.
     bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad != 128 &&   // no persistent m_pad 128 instance
                       kbt % split_k == 0 && split_k != 3;
-    bool alias = choose_alias(m_pad, split_k);
     int tiles = (N + tile_n - 1) / tile_n;            // the last tile may be partial
     int clusters = tiles;
-    Ring ring = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, alias);
-    if (stages_override >= 2)
-        ring.stages = stages_override;
-    int fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1, alias);
+    bool alias = false;
+    Ring ring;
+    int fp = 0;
+    // The ring (and the mailbox placement) for one tile width: with the
+    // mailbox in the ring when that is fixed, else whichever placement fits
+    // the larger W ring (the separate mailbox on a tie: no hand-off needed).
+    auto pick = [&]() {
+        const int fa = forced_alias(m_pad, split_k);
+        auto one = [&](bool al, Ring &r, int &f) {
+            r = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, al);
+            if (stages_override >= 2)
+                r.stages = stages_override;
+            f = footprint(tile_n, m_pad, split_k, r.stages, r.kbs, 1, al);
+        };
+        if (fa >= 0) {
+            alias = fa == 1;
+            one(alias, ring, fp);
+            return;
+        }
+        Ring r0, r1;
+        int f0 = 0, f1 = 0;
+        one(false, r0, f0);
+        one(true, r1, f1);
+        const long long w0 = f0 <= kMaxSmemPerCta ? (long long)r0.kbs * r0.stages : -1;
+        const long long w1 = f1 <= kMaxSmemPerCta ? (long long)r1.kbs * r1.stages : -1;
+        alias = w1 > w0;
+        ring = alias ? r1 : r0;
+        fp = alias ? f1 : f0;
+    };
+    pick();
     if (tile_n == 128 && (fp > kMaxSmemPerCta || !kernel_for(tile_n, m_pad, split_k, false))) {
         // e.g. m_pad 64 with split_k 8: the 128-column mailbox does not fit, or
         // m_pad 128 with split_k 4: no 128-column instance; use 64 columns
         tile_n = 64;
         m_pad = m_pad_of(M);
-        alias = choose_alias(m_pad, split_k);
         tiles = (N + tile_n - 1) / tile_n;
         clusters = tiles;
-        ring = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, alias);
-        if (stages_override >= 2)
-            ring.stages = stages_override;
-        fp = footprint(tile_n, m_pad, split_k, ring.stages, ring.kbs, 1, alias);
+        pick();
     }
     if (fp > kMaxSmemPerCta || !kernel_for(tile_n, m_pad, split_k, false))
         return LOWM_ERR_UNSUPPORTED_SHAPE;
@@ -481,12 +516,15 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     t->mbox_in_ring = alias ? 1 : 0;
     // W stages requested ahead of the programmatic-dependency wait when the
     // caller promises that the preceding kernel does not write W: the whole
-    // ring, except for rings of three or more 64-column stages (M <= 8 at
-    // N 6144, K 4096), where one stage measured fastest on GB300 (9.95 us
-    // against 10.51 us for the whole ring at M4 N6144 K4096; the whole ring
-    // was fastest for every other shape of the sweep).  LOWM_W_PREFETCH
-    // overrides (tuning).
-    int wpf = (!persistent && tile_n == 64 && stages >= 3) ? 1 : stages;
+    // ring, except for rings of three or more 64-column stages on a grid
+    // that overflows the SMs, where one stage measured fastest on GB300 (64
+    // columns at M4 N6144 K4096, 192 CTAs: 9.95 us against 10.51 us for the
+    // whole ring; the ring's next-GEMM requests otherwise slow the running
+    // GEMM's tail).  With one CTA per SM the whole ring is best (M4 N6144 K4096
+    // on a 4 x 3 128-column ring: 8.90 us against 9.81 with two stages and
+    // 10.74 with one; M4 N2304 K12288 on an 8 x 3 ring: 9.98 against 10.73
+    // with one).  LOWM_W_PREFETCH overrides (tuning).
+    int wpf = (!persistent && tile_n == 64 && stages >= 3 && clusters * split_k > nsm) ? 1 : stages;
     const int force_wpf = env_int("LOWM_W_PREFETCH", -1);
     if (force_wpf >= 0)
         wpf = std::min(force_wpf, stages);

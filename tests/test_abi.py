@@ -59,13 +59,15 @@ def test_shipped_tactic_is_reproduced(L, monkeypatch):
 
 
 def test_default_tactic_for_the_headline_workload(L):
-    # GB300 with the one-stage L2 prefetch: 128-column tiles, one CTA per SM
-    # on 96 SMs (9.43 us) beat the 64-column tiles on 192 CTAs (10.14 us).
+    # GB300: 128-column tiles, one CTA per SM on 96 SMs, a 4 x 3 ring (192 KiB
+    # of W) that fits only with the mailbox in the ring, the whole ring
+    # requested before the dependency wait: 8.90 us, against 9.53 us for the
+    # 4 x 2 ring and 10.14 us for 64-column tiles on 192 CTAs.
     st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
     assert st == lowm.LOWM_OK
-    assert (t["tile_n"], t["m_pad"], t["split_k"], t["kb_per_stage"], t["stages"]) == (128, 16, 2, 4, 2)
+    assert (t["tile_n"], t["m_pad"], t["split_k"], t["kb_per_stage"], t["stages"]) == (128, 16, 2, 4, 3)
     assert t["num_clusters"] == 48 and t["ctas"] == 96 and t["persistent"] == 0 and t["smem_bytes"] <= 232448
-    assert t["l2_prefetch_stages"] == 1 and t["mbox_in_ring"] == 0
+    assert t["l2_prefetch_stages"] == 1 and t["mbox_in_ring"] == 1 and t["w_prefetch_stages"] == 3
 
 
 @pytest.mark.parametrize("M,N,K,sk,tile", [
@@ -108,14 +110,27 @@ def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
         assert t["num_clusters"] == t["tiles"] and t["tiles_per_cluster"] == 1
 
 
-@pytest.mark.parametrize("M,N,K,sk,kbs,stages", [
-    # the 64-column ring each workload measured fastest with on GB300 (tactic sweep)
-    (4, 6144, 4096, 2, 4, 3), (4, 2304, 12288, 4, 8, 2), (4, 49152, 4096, 2, 2, 2), (4, 49152, 4096, 1, 4, 2),
-    (16, 6144, 32768, 4, 2, 2)])   # (M16 now defaults to 128-column tiles; this pins the 64-column ring)
-def test_ring_matches_the_measured_best(L, M, N, K, sk, kbs, stages, monkeypatch):
-    monkeypatch.setenv("LOWM_TILE_N", "64")
+@pytest.mark.parametrize("M,N,K,sk,tile,kbs,stages,alias", [
+    # the ring (and mailbox placement) each workload measured fastest with on GB300 (tactic sweeps)
+    (4, 6144, 4096, 2, 128, 4, 3, 1),       # 8.90 us; 4 x 2 next to the mailbox 9.53 us
+    (64, 6144, 4096, 2, 128, 4, 2, 1),      # 10.66 us; 2 x 3 next to the mailbox 10.97 us
+    (128, 6144, 4096, 2, 128, 2, 3, 1),     # 13.2 us; 2 x 2 next to the mailbox 16.4 us
+    (4, 2304, 12288, 4, 64, 8, 3, 0),       # one CTA per SM: 9.98 us (whole ring before the PDL wait); 8 x 2 10.06 us
+    (4, 49152, 4096, 2, 64, 2, 2, 0), (4, 49152, 4096, 1, 64, 4, 2, 0),
+    (16, 6144, 32768, 4, 64, 2, 3, 1)])     # 64.1 us; 2 x 2 next to the mailbox 63.9 us (within noise)
+def test_ring_matches_the_measured_best(L, M, N, K, sk, tile, kbs, stages, alias):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
-    assert st == lowm.LOWM_OK and (t["tile_n"], t["kb_per_stage"], t["stages"]) == (64, kbs, stages)
+    assert st == lowm.LOWM_OK
+    assert (t["tile_n"], t["kb_per_stage"], t["stages"], t["mbox_in_ring"]) == (tile, kbs, stages, alias)
+
+
+def test_64_column_rings_with_several_ctas_per_sm_stay_capped(L, monkeypatch):
+    # Grids with several CTAs per SM keep at most 160 KiB of W per ring
+    # (the one-wave M4 N6144 K4096 ring on 64 columns is 4 x 3 = 96 KiB).
+    monkeypatch.setenv("LOWM_TILE_N", "64")
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and (t["tile_n"], t["kb_per_stage"], t["stages"]) == (64, 4, 3)
+    assert t["kb_per_stage"] * t["stages"] * 64 * 64 * 2 <= 160 * 1024
 
 
 @pytest.mark.parametrize("M,N,K,sk", [(4, 256, 64 * 3, 1), (4, 256, 64 * 6, 1), (4, 256, 64 * 5, 1),
@@ -162,9 +177,10 @@ def test_any_n_is_tiled_with_a_partial_last_tile(L, M, N, K, sk):
 
 
 @pytest.mark.parametrize("M,N,K,sk,wpf", [
-    # one W stage ahead of the PDL wait for three-stage 64-column rings, the whole ring otherwise (GB300 sweep)
-    (4, 6152, 4096, 2, 1), (4, 6144, 4096, 2, 2), (8, 6144, 4096, 2, 2), (4, 2304, 12288, 4, 2), (4, 49152, 4096, 2, 2),
-    (16, 6144, 32768, 4, 2), (64, 6144, 4096, 2, 3), (32, 6144, 4096, 2, 2)])
+    # one W stage ahead of the PDL wait for three-stage 64-column rings on a grid that overflows
+    # the SMs, the whole ring otherwise (GB300 sweeps)
+    (4, 6152, 4096, 2, 1), (4, 6144, 4096, 2, 3), (8, 6144, 4096, 2, 3), (4, 2304, 12288, 4, 3), (4, 49152, 4096, 2, 2),
+    (16, 6144, 32768, 4, 1), (64, 6144, 4096, 2, 2), (32, 6144, 4096, 2, 2)])
 def test_two_mma_issuers_and_prefetch_depth(L, M, N, K, sk, wpf):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
     assert st == lowm.LOWM_OK and t["mma_issuers"] == 2 and t["persistent"] == 0
@@ -323,8 +339,10 @@ def test_uneven_k_shares_are_accepted(L, K, sk):
 def test_split3_defaults_to_the_mailbox_in_the_ring(L, monkeypatch):
     st, t = lowm.lowm_gemm_query_tactic(64, 6144, 4096, 3)
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1
-    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    st, t = lowm.lowm_gemm_query_tactic(4, 6152, 4096, 2)       # a mailbox of 2 KiB: no larger ring to gain
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0
+    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)       # sharing the ring makes room for a third stage
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1 and t["stages"] == 3
     monkeypatch.setenv("LOWM_MBOX_IN_RING", "0")
     st, t = lowm.lowm_gemm_query_tactic(4, 640, 64 * 9, 3)
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0

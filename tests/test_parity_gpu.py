@@ -720,3 +720,42 @@ def test_split3_twenty_launches_are_bitwise_identical(M, N, K):
     sync_ok()
     o = outs.view(torch.int16)
     assert bool((o == o[0:1]).all())
+
+
+# ---------------------------------------------------------------- seeded fuzz over uneven K shares, the mailbox placement and the L2 prefetch
+def _fuzz_cases_uneven(n=40, seed=20261203):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        M = int(rng.choice([1, 3, 4, 8, 9, 16, 17, 32, 40, 64, 65, 96, 128]))
+        sk = int(rng.choice([2, 3, 4, 8]))
+        K = 64 * int(rng.integers(sk, 9 * sk + 1))           # any block count with a non-empty share per rank
+        N = int(rng.choice([int(rng.integers(1, 600)), 128 * int(rng.integers(1, 8))]))
+        env = {"LOWM_TILE_N": str(int(rng.choice([0, 64, 128]))),
+               "LOWM_KB_PER_STAGE": str(int(rng.choice([0, 1, 2, 4]))),
+               "LOWM_MBOX_IN_RING": str(int(rng.choice([-1, 0, 1]))),
+               "LOWM_L2_PREFETCH": str(int(rng.choice([-1, 0, 1, 2, 3])))}
+        cases.append((M, N, K, sk, env, int(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_fuzz_uneven_splits_mailbox_and_prefetch(case, monkeypatch):
+    M, N, K, sk, env, flags = _fuzz_cases_uneven()[case]
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    if st == lowm.LOWM_ERR_UNSUPPORTED_SHAPE:
+        # only a mailbox that cannot fit next to the ring may be refused
+        assert M > 64 or env["LOWM_MBOX_IN_RING"] == "0"
+        pytest.skip("refused by the host before any launch: %s" % lowm.status_string(st))
+    assert st == lowm.LOWM_OK
+    A, W = inputs.make_problem(M, N, K, seed=1500 + case)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    F = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    assert lowm.lowm_gemm_bf16_debug(Ad, Wd, C, M, N, K, sk, None, c_f32=F, flags=flags) == lowm.LOWM_OK
+    sync_ok()
+    Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
+    assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, A, W,
+                  label="fuzz-uneven %d" % case)
