@@ -344,7 +344,7 @@ def run_ours(args):
     # LOWM_FLAG_W_BEFORE_PDL_WAIT holds; --default-launch measures the plain
     # lowm_gemm_bf16 path instead (also reported under "variants").
     w = dict(WORKLOAD, flags=0 if args.default_launch else lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
-    st, tactic = lowm.lowm_gemm_query_tactic(w["M"], w["N"], w["K"], w["split_k"])
+    st, tactic = lowm.lowm_gemm_query_tactic_ex(w["M"], w["N"], w["K"], w["split_k"], w["flags"])
     assert st == 0, lowm.status_string(st)
     peak, peak_kind = measured_peak()
     bytes_per = algo_bytes(w["M"], w["N"], w["K"])
@@ -368,7 +368,7 @@ def run_ours(args):
     wide_w = dict(WIDE, flags=w["flags"])
     wsecs, _, wR = time_device(lowm, wide_w, wide_steps, max(args.warmup, 3), device)
     wbytes = algo_bytes(WIDE["M"], WIDE["N"], WIDE["K"])
-    _, wtactic = lowm.lowm_gemm_query_tactic(WIDE["M"], WIDE["N"], WIDE["K"], WIDE["split_k"])
+    _, wtactic = lowm.lowm_gemm_query_tactic_ex(WIDE["M"], WIDE["N"], WIDE["K"], WIDE["split_k"], w["flags"])
     wide = {"workload": workload_name(WIDE), "us_per_gemm": wsecs / wide_steps * 1e6, "tactic": wtactic,
             "traffic": committed_traffic(WIDE, wtactic),
             "gbs": wbytes * wide_steps / wsecs / 1e9, "steps": wide_steps,
@@ -392,7 +392,7 @@ def run_ours(args):
     osteps = max(200, min(args.steps, 5000))
     for name, (M, N, K, sk) in OTHER_CONFIGS:
         ow = dict(M=M, N=N, K=K, split_k=sk, flags=w["flags"])
-        _, otactic = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+        _, otactic = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, w["flags"])
         steps_o = osteps if N * K <= 64 << 20 else max(200, osteps // 5)
         osecs, _, _ = time_device(lowm, ow, steps_o, max(args.warmup, 3), device)
         ob = algo_bytes(M, N, K)
@@ -520,7 +520,8 @@ def run_reference(args):
 
 
 def run_profile_case(args):
-    """Plain launches of the workload for ncu: `warmup` + `steps` GEMMs, rotating W copies, no graphs."""
+    """Plain launches of the workload for ncu: `warmup` + `steps` GEMMs, rotating W copies, no graphs,
+    through lowm_gemm_bf16_ex with the flags the benchmark times (W-before-PDL unless --default-launch)."""
     import __graft_entry__
     __graft_entry__.build()
     from split_bf16_gemm_swap_gb300 import inputs, lowm
@@ -537,8 +538,9 @@ def run_profile_case(args):
     Ws = [W.to(device) for _ in range(R)]
     C = torch.empty((M, N), dtype=torch.bfloat16, device=device)
     torch.cuda.synchronize()
+    flags = 0 if args.default_launch else lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT   # the launch the bench times
     for i in range(args.warmup + args.steps):
-        st = lowm.lowm_gemm_bf16(Ad, Ws[i % R], C, M, N, K, sk, None)
+        st = lowm.lowm_gemm_bf16_ex(Ad, Ws[i % R], C, M, N, K, sk, flags, None)
         assert st == 0, lowm.status_string(st)
     st, detail = lowm.lowm_gemm_sync_status()
     assert st == 0, "kernel status bits %#x" % detail

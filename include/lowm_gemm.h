@@ -176,6 +176,16 @@ lowm_status_t lowm_gemm_bf16_ex(const void *A, const void *W, void *C,
  */
 lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tactic_t *out);
 
+/*
+ * The tactic lowm_gemm_bf16_ex launches with these flags (LOWM_FLAG_*; unknown
+ * bits are rejected with LOWM_ERR_INVALID_ARGUMENT).  The choice depends on
+ * the W promise: with LOWM_FLAG_W_BEFORE_PDL_WAIT and one CTA per SM the ring
+ * may fill the SM's shared memory (its first stages are requested before the
+ * dependency wait), without it the ring holds at most 160 KiB of W.
+ * lowm_gemm_query_tactic is this call with flags 0.
+ */
+lowm_status_t lowm_gemm_query_tactic_ex(int M, int N, int K, int split_k, unsigned int flags, lowm_tactic_t *out);
+
 /* A static, human-readable name for a status code (never NULL).  The pages'
  * kernel reports no errors, so this helper of the boundary has no passage
  * behind it. */

@@ -9,5 +9,5 @@ missing.
 from .lowm import (  # noqa: F401
     ABI_FUNCTIONS, LOWM_FLAG_W_BEFORE_PDL_WAIT, LOWM_OK, LowmError, gemm, lowm_gemm_bf16, lowm_gemm_bf16_debug,
     lowm_gemm_bf16_ex, lowm_gemm_bf16_host,
-    lowm_gemm_query_tactic, lowm_gemm_sync_status, lowm_status_string, lowm_tmem_hog_launch,
+    lowm_gemm_query_tactic, lowm_gemm_query_tactic_ex, lowm_gemm_sync_status, lowm_status_string, lowm_tmem_hog_launch,
 )

@@ -167,15 +167,20 @@ struct Ring {
 
 constexpr int kMaxRingBytes = 160 * 1024;     // W bytes per ring when several CTAs share an SM
 
-Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int sms, int bufs, bool alias = false)
+Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int sms, int bufs, bool alias = false,
+                 bool w_promise = false)
 {
     const int per_sm_one_wave = (ctas + std::max(1, sms) - 1) / std::max(1, sms);
     const int per_sm = per_sm_one_wave <= 4 ? std::max(1, per_sm_one_wave) : (split_k == 1 ? 3 : 5);
     const int budget = std::min(kMaxSmemPerCta, kSmemPerSm / per_sm - kSmemReservedPerCta);
-    // One CTA per SM: the ring may take all of the SM's shared memory (a
-    // 128-column M4 N6144 K4096 CTA with a 4 x 3 ring, 192 KiB of W, measured
-    // 8.90 us against 9.57 us with the 4 x 2 ring the 160 KiB cap allowed).
-    const int cap = per_sm == 1 ? kMaxSmemPerCta : kMaxRingBytes;
+    // One CTA per SM, with the caller's W promise (the first ring of W is
+    // requested before the dependency wait): the ring may take all of the
+    // SM's shared memory (a 128-column M4 N6144 K4096 CTA with a 4 x 3 ring,
+    // 192 KiB of W, measured 8.90 us against 9.57 us with the 4 x 2 ring the
+    // 160 KiB cap allows).  Without the promise the deeper rings measured
+    // slower (4 x 3 11.17 against 4 x 2 10.67 us; M4 N2304 K12288 8 x 3 12.13
+    // against 8 x 2 11.67 us), so the cap stays.
+    const int cap = (per_sm == 1 && w_promise) ? kMaxSmemPerCta : kMaxRingBytes;
     int force_kbs = env_int("LOWM_KB_PER_STAGE", 0);
     if (force_kbs != 1 && force_kbs != 2 && force_kbs != 4 && force_kbs != 8)
         force_kbs = 0;
@@ -412,7 +417,7 @@ int resident_clusters(int tile_n, int m_pad, int split_k, int smem, int sms, boo
     return n;
 }
 
-lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_device, int stages_override,
+lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_device, unsigned flags, int stages_override,
                           int full_smem, lowm_tactic_t *t)
 {
     if (M <= 0 || N <= 0 || K <= 0 || split_k < 0)
@@ -427,6 +432,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     if (stages_override == 1)
         return LOWM_ERR_INVALID_ARGUMENT;
     const int nsm = sms > 0 ? sms : 152;
+    const bool w_promise = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) != 0;
     int tile_n = choose_tile_n(N, K, split_k, nsm);
     int m_pad = m_pad_for(M, tile_n);
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1); it splits K evenly.
@@ -441,9 +447,14 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     // mailbox in the ring when that is fixed, else whichever placement fits
     // the larger W ring (the separate mailbox on a tie: no hand-off needed).
     auto pick = [&]() {
-        const int fa = forced_alias(m_pad, split_k);
+        // Without the W promise the mailbox shares the ring only where it must
+        // (M64 N6144 K4096 with default flags: 2 x 3 next to the mailbox 12.17
+        // us against 4 x 2 in the ring 12.36 us).
+        int fa = forced_alias(m_pad, split_k);
+        if (fa < 0 && !w_promise)
+            fa = 0;
         auto one = [&](bool al, Ring &r, int &f) {
-            r = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, al);
+            r = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, al, w_promise);
             if (stages_override >= 2)
                 r.stages = stages_override;
             f = footprint(tile_n, m_pad, split_k, r.stages, r.kbs, 1, al);
@@ -634,7 +645,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     if (st != LOWM_OK)
         return st;
     lowm_tactic_t t;
-    st = make_tactic(M, N, K, split_k, sms, true, dbg ? dbg->stages : 0, (dbg && dbg->full_smem) ? 1 : 0, &t);
+    st = make_tactic(M, N, K, split_k, sms, true, flags, dbg ? dbg->stages : 0, (dbg && dbg->full_smem) ? 1 : 0, &t);
     if (st != LOWM_OK)
         return st;
     KernelFn fn = kernel_for(t.tile_n, t.m_pad, t.split_k, t.persistent != 0);
@@ -741,7 +752,14 @@ lowm_status_t lowm_gemm_bf16_debug(const void *A, const void *W, void *C, int M,
 
 lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tactic_t *out)
 {
+    return lowm_gemm_query_tactic_ex(M, N, K, split_k, 0u, out);
+}
+
+lowm_status_t lowm_gemm_query_tactic_ex(int M, int N, int K, int split_k, unsigned int flags, lowm_tactic_t *out)
+{
     if (!out)
+        return LOWM_ERR_INVALID_ARGUMENT;
+    if (flags & ~LOWM_FLAG_W_BEFORE_PDL_WAIT)
         return LOWM_ERR_INVALID_ARGUMENT;
     // Host-only query: with a usable sm_103 device current, the same numbers the
     // launch uses; otherwise the per-SM arithmetic for a 152-SM GB300.
@@ -755,7 +773,7 @@ lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tact
         sms = 152;
     }
     lowm_tactic_t t;
-    const lowm_status_t st = make_tactic(M, N, K, split_k, sms, have_device, 0, 0, &t);
+    const lowm_status_t st = make_tactic(M, N, K, split_k, sms, have_device, flags, 0, 0, &t);
     if (st == LOWM_OK)
         *out = t;
     return st;
@@ -802,7 +820,7 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
     lowm_status_t st = check_device(&sms);
     if (st != LOWM_OK)
         return st;
-    if ((st = make_tactic(M, N, K, split_k, sms, true, 0, 0, &t)) != LOWM_OK)
+    if ((st = make_tactic(M, N, K, split_k, sms, true, 0u, 0, 0, &t)) != LOWM_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(A_dev, A_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||

@@ -30,6 +30,7 @@ ABI_FUNCTIONS = (
     "lowm_gemm_bf16",
     "lowm_gemm_bf16_ex",
     "lowm_gemm_query_tactic",
+    "lowm_gemm_query_tactic_ex",
     "lowm_status_string",
     "lowm_gemm_sync_status",
     "lowm_gemm_bf16_host",
@@ -88,6 +89,8 @@ def lib():
         L.lowm_gemm_bf16_ex.restype = st
         L.lowm_gemm_query_tactic.argtypes = [i, i, i, i, ctypes.POINTER(lowm_tactic_t)]
         L.lowm_gemm_query_tactic.restype = st
+        L.lowm_gemm_query_tactic_ex.argtypes = [i, i, i, i, ctypes.c_uint, ctypes.POINTER(lowm_tactic_t)]
+        L.lowm_gemm_query_tactic_ex.restype = st
         L.lowm_status_string.argtypes = [st]
         L.lowm_status_string.restype = ctypes.c_char_p
         L.lowm_gemm_sync_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -140,6 +143,13 @@ def lowm_gemm_query_tactic(M: int, N: int, K: int, split_k: int = 0):
     """Return ``(status, tactic dict or None)``."""
     t = lowm_tactic_t()
     s = lib().lowm_gemm_query_tactic(int(M), int(N), int(K), int(split_k), ctypes.byref(t))
+    return s, (t.as_dict() if s == LOWM_OK else None)
+
+
+def lowm_gemm_query_tactic_ex(M: int, N: int, K: int, split_k: int = 0, flags: int = 0):
+    """Return ``(status, tactic dict or None)`` for a launch with these flags."""
+    t = lowm_tactic_t()
+    s = lib().lowm_gemm_query_tactic_ex(int(M), int(N), int(K), int(split_k), int(flags), ctypes.byref(t))
     return s, (t.as_dict() if s == LOWM_OK else None)
 
 

@@ -60,9 +60,9 @@ def capture(M: int, N: int, K: int, split_k: int, flags: int, launches: int, see
     """Run the graph of `launches` GEMMs twice and return the second replay's timestamps (ns)."""
     import torch
     from . import inputs, lowm
-    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, split_k, flags)
     if st != lowm.LOWM_OK:
-        raise lowm.LowmError(st, "lowm_gemm_query_tactic")
+        raise lowm.LowmError(st, "lowm_gemm_query_tactic_ex")
     ctas = t["ctas"]
     A, W = inputs.make_problem(M, N, K, seed=seed)
     Ad = A.cuda()

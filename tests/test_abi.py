@@ -63,11 +63,15 @@ def test_default_tactic_for_the_headline_workload(L):
     # of W) that fits only with the mailbox in the ring, the whole ring
     # requested before the dependency wait: 8.90 us, against 9.53 us for the
     # 4 x 2 ring and 10.14 us for 64-column tiles on 192 CTAs.
-    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     assert st == lowm.LOWM_OK
     assert (t["tile_n"], t["m_pad"], t["split_k"], t["kb_per_stage"], t["stages"]) == (128, 16, 2, 4, 3)
     assert t["num_clusters"] == 48 and t["ctas"] == 96 and t["persistent"] == 0 and t["smem_bytes"] <= 232448
     assert t["l2_prefetch_stages"] == 1 and t["mbox_in_ring"] == 1 and t["w_prefetch_stages"] == 3
+    # Without the W promise (lowm_gemm_bf16) the deeper ring measured slower: the 4 x 2 ring next to the
+    # mailbox, 10.67 us against 11.17 us.
+    st, t0 = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    assert st == lowm.LOWM_OK and (t0["tile_n"], t0["kb_per_stage"], t0["stages"], t0["mbox_in_ring"]) == (128, 4, 2, 0)
 
 
 @pytest.mark.parametrize("M,N,K,sk,tile", [
@@ -119,9 +123,26 @@ def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
     (4, 49152, 4096, 2, 64, 2, 2, 0), (4, 49152, 4096, 1, 64, 4, 2, 0),
     (16, 6144, 32768, 4, 64, 2, 3, 1)])     # 64.1 us; 2 x 2 next to the mailbox 63.9 us (within noise)
 def test_ring_matches_the_measured_best(L, M, N, K, sk, tile, kbs, stages, alias):
+    # the benchmark's launches carry the W-before-PDL promise
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    assert st == lowm.LOWM_OK
+    assert (t["tile_n"], t["kb_per_stage"], t["stages"], t["mbox_in_ring"]) == (tile, kbs, stages, alias)
+
+
+@pytest.mark.parametrize("M,N,K,sk,tile,kbs,stages,alias", [
+    # without the W promise (default flags, GB300 sweep): the rings within 160 KiB of W
+    (4, 6144, 4096, 2, 128, 4, 2, 0),       # 10.67 us; 4 x 3 in the ring 11.17 us
+    (64, 6144, 4096, 2, 128, 2, 3, 0),      # 12.17 us; 4 x 2 in the ring 12.36 us
+    (4, 2304, 12288, 4, 64, 8, 2, 0)])      # 11.67 us; 8 x 3 12.13 us
+def test_ring_without_the_w_promise(L, M, N, K, sk, tile, kbs, stages, alias):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
     assert st == lowm.LOWM_OK
     assert (t["tile_n"], t["kb_per_stage"], t["stages"], t["mbox_in_ring"]) == (tile, kbs, stages, alias)
+
+
+def test_query_with_unknown_flags_is_rejected(L):
+    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, 2)
+    assert st == lowm.LOWM_ERR_INVALID_ARGUMENT and t is None
 
 
 def test_64_column_rings_with_several_ctas_per_sm_stay_capped(L, monkeypatch):
@@ -182,7 +203,7 @@ def test_any_n_is_tiled_with_a_partial_last_tile(L, M, N, K, sk):
     (4, 6152, 4096, 2, 1), (4, 6144, 4096, 2, 3), (8, 6144, 4096, 2, 3), (4, 2304, 12288, 4, 3), (4, 49152, 4096, 2, 2),
     (16, 6144, 32768, 4, 1), (64, 6144, 4096, 2, 2), (32, 6144, 4096, 2, 2)])
 def test_two_mma_issuers_and_prefetch_depth(L, M, N, K, sk, wpf):
-    st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     assert st == lowm.LOWM_OK and t["mma_issuers"] == 2 and t["persistent"] == 0
     assert t["w_prefetch_stages"] == wpf <= t["stages"]
 
@@ -341,7 +362,7 @@ def test_split3_defaults_to_the_mailbox_in_the_ring(L, monkeypatch):
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1
     st, t = lowm.lowm_gemm_query_tactic(4, 6152, 4096, 2)       # a mailbox of 2 KiB: no larger ring to gain
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0
-    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)       # sharing the ring makes room for a third stage
+    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, 1)  # sharing the ring makes room for a third stage
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1 and t["stages"] == 3
     monkeypatch.setenv("LOWM_MBOX_IN_RING", "0")
     st, t = lowm.lowm_gemm_query_tactic(4, 640, 64 * 9, 3)

@@ -53,9 +53,9 @@ def run_gpu(A, W, split_k=0, want_f32=True, **dbg):
     return inputs.bits(C.cpu()), (F.cpu().numpy().astype(np.float64) if F is not None else None)
 
 
-def check(A, W, split_k=0, exact=False):
+def check(A, W, split_k=0, exact=False, flags=0):
     M, K = A.shape
-    C, F = run_gpu(A, W, split_k)
+    C, F = run_gpu(A, W, split_k, flags=flags)
     Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
     if exact:
         bad = np.argwhere(C != Cref)
@@ -759,3 +759,20 @@ def test_fuzz_uneven_splits_mailbox_and_prefetch(case, monkeypatch):
     Cref, S = oracle.gemm_bf16_f64(inputs.bits(A), inputs.bits(W))
     assert_parity(inputs.bits(C.cpu()), F.cpu().numpy().astype(np.float64), Cref, S, A, W,
                   label="fuzz-uneven %d" % case)
+
+
+# ---------------------------------------------------------------- the timed launches: with the W-before-PDL promise
+@pytest.mark.parametrize("M,N,K,split_k,kind", [
+    (4, 6144, 4096, 2, "randn"), (4, 2304, 12288, 4, "randn"), (4, 49152, 4096, 2, "randn"),
+    (16, 6144, 32768, 4, "int"), (1, 6144, 4096, 0, "randn"), (16, 6144, 4096, 0, "randn"),
+    (32, 6144, 4096, 0, "randn"), (64, 6144, 4096, 0, "randn"), (128, 6144, 4096, 0, "randn")])
+def test_workloads_with_the_w_promise(M, N, K, split_k, kind):
+    # The tactic the benchmark times (lowm_gemm_bf16_ex with
+    # LOWM_FLAG_W_BEFORE_PDL_WAIT: deeper rings, the mailbox in the ring)
+    # against the oracle, and bitwise equal to the launch without the flag.
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, split_k, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    assert st == lowm.LOWM_OK
+    A, W = inputs.make_problem(M, N, K, seed=1800 + M, kind=kind)
+    C1 = check(A, W, split_k, exact=(kind == "int"), flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    C0, _ = run_gpu(A, W, split_k, want_f32=False)
+    assert np.array_equal(C0, C1)

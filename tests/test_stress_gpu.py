@@ -39,8 +39,8 @@ def _lib():
     lowm.lib()
 
 
-def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0, warp_mask=STALL_WARPS):
-    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0, warp_mask=STALL_WARPS, flags=0):
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, split_k, flags)
     assert st == lowm.LOWM_OK
     ctas = t["ctas"]
     s_gemm = torch.cuda.Stream()
@@ -52,7 +52,8 @@ def stressed(Ad, Wd, M, N, K, split_k, stall_ns, hog_cols=256, stall_rank_mask=0
         for _ in range(3):
             assert lowm.lowm_tmem_hog_launch(s_hog, 4096, hog_cols, 4) == lowm.LOWM_OK
         st = lowm.lowm_gemm_bf16_debug(Ad, Wd, outs[i], M, N, K, split_k, s_gemm, stall_warp_mask=warp_mask,
-                                       stall_rank_mask=stall_rank_mask, stall_ns=stall_ns, probes=probes[i])
+                                       stall_rank_mask=stall_rank_mask, stall_ns=stall_ns, probes=probes[i],
+                                       flags=flags)
         assert st == lowm.LOWM_OK
     torch.cuda.synchronize()
     st, detail = lowm.lowm_gemm_sync_status(s_gemm)
@@ -163,3 +164,24 @@ def test_persistent_schedule_under_stress(tile, monkeypatch):
     outs, probes = stressed(Ad, Wd, M, N, K, split_k, 10_000)
     assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
     check_probes(probes)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (64, 6144, 4096, 2), (16, 6144, 32768, 4)])
+def test_stress_with_the_w_promise(M, N, K, split_k):
+    # The timed tactics (LOWM_FLAG_W_BEFORE_PDL_WAIT: the deeper rings with the
+    # mailbox in the ring, W requested before the dependency wait) under the
+    # same stall + TMEM hog method.
+    flags = lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, split_k, flags)
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1
+    A, W = inputs.make_problem(M, N, K, seed=1234, kind="int")
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    assert lowm.lowm_gemm_bf16_ex(Ad, Wd, ref, M, N, K, split_k, flags, None) == lowm.LOWM_OK
+    torch.cuda.synchronize()
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(inputs.bits(ref.cpu()), np.broadcast_to(inputs.bits(col[None, :]), (M, N)))
+    for stall_ns in (5_000, 100_000):
+        outs, probes = stressed(Ad, Wd, M, N, K, split_k, stall_ns, flags=flags)
+        assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
+        check_probes(probes)
