@@ -776,3 +776,26 @@ def test_workloads_with_the_w_promise(M, N, K, split_k, kind):
     C1 = check(A, W, split_k, exact=(kind == "int"), flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     C0, _ = run_gpu(A, W, split_k, want_f32=False)
     assert np.array_equal(C0, C1)
+
+
+def test_pdl_chain_with_the_deep_ring_and_w_promise():
+    # C of each GEMM is the next GEMM's A (K = N = 6144), launched back to back
+    # with the W promise: the 128-column tactic with the 4 x 3 ring and the
+    # mailbox in the ring requests W before the dependency wait, and must
+    # still read A only after it.  Each link must equal a separate launch on
+    # the same input, which itself meets the parity bar.
+    M, D = 4, 6144
+    flags = lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, D, D, 2, flags)
+    assert st == lowm.LOWM_OK and t["tile_n"] == 128 and t["mbox_in_ring"] == 1 and t["w_prefetch_stages"] >= 2
+    A0, _ = inputs.make_problem(M, D, D, seed=51)
+    Ws = [inputs.make_problem(M, D, D, seed=60 + i)[1] for i in range(4)]
+    Wd = [w.to(DEV) for w in Ws]
+    Cs = [A0.to(DEV)] + [torch.empty((M, D), dtype=torch.bfloat16, device=DEV) for _ in Ws]
+    for i, w in enumerate(Wd):
+        assert lowm.lowm_gemm_bf16_ex(Cs[i], w, Cs[i + 1], M, D, D, 2, flags, None) == lowm.LOWM_OK
+    sync_ok()
+    for i, w in enumerate(Ws):
+        a = Cs[i].cpu()
+        alone = check(a, w, 2, flags=flags)                # a separate launch on this link's input, vs the oracle
+        assert np.array_equal(inputs.bits(Cs[i + 1].cpu()), alone), "link %d" % i
