@@ -86,9 +86,10 @@ typedef enum {
  *   kb_per_stage 64-wide K blocks per ring stage, fetched by one 3-D TMA
  *                copy of W and one of A (the largest of 8, 4, 2, 1 that
  *                divides the rank's block count and whose two-stage ring
- *                fits both the per-SM shared-memory budget and 160 KiB of
- *                W): a copy has a fixed per-CTA cost, so larger copies are
- *                what let one CTA stream its share of HBM
+ *                fits the per-SM shared-memory budget, and 160 KiB of W
+ *                unless one CTA per SM runs with the W promise): a copy has
+ *                a fixed per-CTA cost, so larger copies are what let one CTA
+ *                stream its share of HBM
  *   mma_issuers  threads issuing tcgen05.mma per CTA: 2 for the one-tile
  *                kernel (one takes the even, the other the odd 16-wide K steps
  *                of every stage, each into its own TMEM accumulator; the
