@@ -104,7 +104,11 @@ typedef enum {
  *                last MMA has completed (the owner then tells each peer that
  *                its mailbox is open); a CTA needs max(ring, mailbox) bytes of
  *                shared memory instead of their sum.  0: the mailbox sits
- *                after the ring.
+ *                after the ring; at m_pad 64 with split_k 2 the exchange is
+ *                then a reduce-scatter: each rank sends the other rank its
+ *                partial of the other half of the m_pad rows, adds the other
+ *                rank's partial of its own half (the rank-ordered sum of two
+ *                terms) and stores those rows of C.
  *   l2_prefetch_stages  stages of W the producer requests into L2 (TMA
  *                prefetch, no shared-memory destination) ahead of its newest
  *                ring load, so that one more stage of W is in flight than the
@@ -239,6 +243,8 @@ lowm_status_t lowm_gemm_bf16_host(const void *A_host, const void *W_host, void *
  *   drop_mailbox     1: the non-owner ranks skip their mailbox publication, so
  *                    the owner's mailbox wait runs out (a dropped message, to
  *                    test the timeout path); the output is then undefined.
+ *                    In the reduce-scatter exchange every rank skips its
+ *                    publication and every rank's wait runs out.
  *                    After a mailbox wait runs out, the owner waits once more
  *                    with the same bound before it exits, so that a peer that
  *                    is only slow lands its partial tile while the owner's

@@ -258,8 +258,10 @@ int m_pad_for(int M, int tile_n)
 // ring's room (M128 N6144 K4096 split_k 2 on 128-column tiles: 14.4 us
 // against 16.4 us with the mailbox next to the ring), and otherwise whenever
 // sharing lets the ring hold more W (make_tactic compares both layouts; M4
-// N6144 K4096: a 4 x 3 ring, 8.90 us, against 4 x 2, 9.57 us; M64 4 x 2
-// against 2 x 3, 10.66 against 10.97 us).  LOWM_MBOX_IN_RING = 0 / 1
+// N6144 K4096: a 4 x 3 ring, 8.90 us, against 4 x 2, 9.57 us).  At m_pad 64
+// with split_k 2 the separate mailbox is the reduce-scatter one, half the
+// size, and already fits the 4 x 2 ring (9.88 us against 10.66 us for the
+// same ring with the mailbox inside it).  LOWM_MBOX_IN_RING = 0 / 1
 // overrides (tuning).  Returns 1 / 0 when the choice is fixed, -1 when the
 // ring sizes decide.
 int forced_alias(int m_pad, int split_k)
@@ -450,8 +452,9 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     // the larger W ring (the separate mailbox on a tie: no hand-off needed).
     auto pick = [&]() {
         // Without the W promise the mailbox shares the ring only where it must
-        // (M64 N6144 K4096 with default flags: 2 x 3 next to the mailbox 12.17
-        // us against 4 x 2 in the ring 12.36 us).
+        // (M64 N6144 K4096 with default flags, before the reduce-scatter
+        // mailbox: 2 x 3 next to the mailbox 12.17 us against 4 x 2 in the
+        // ring 12.36 us).
         int fa = forced_alias(m_pad, split_k);
         if (fa < 0 && !w_promise)
             fa = 0;

@@ -48,6 +48,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -126,6 +127,21 @@ struct SmemLayout {
 // writes the owner's mailbox only after the owner has said so; see
 // lowm_splitk_kernel), so a split-K CTA needs max(ring, mailbox + staging)
 // bytes rather than their sum.
+// Split-K 2 at m_pad 64 with the mailbox next to the ring reduces and
+// scatters: rank q keeps rows [32 q, 32 q + 32) of the tile, sends the other
+// half of its partial to the other rank, sums its own half in rank order and
+// stores it.  Both directions of the cluster link carry 16 KiB (128-column
+// tiles) at once instead of one carrying 32 KiB, neither rank waits for the
+// other's ring to drain, and the halved mailbox and staging leave room for a
+// 4 x 2 ring next to them (GB300, M64 N6144 K4096: 10.66 -> 9.88 us with the W
+// promise, 12.15 -> 11.43 us without; M48 10.56 -> 9.85 us).  At m_pad 32 it
+// measured 9.59 -> 9.66 us with the promise (11.14 -> 10.79 without) and is
+// not used.
+__host__ __device__ constexpr bool reduce_scatter_of(int m_pad, int split_k, int bufs, bool mbox_in_ring)
+{
+    return split_k == 2 && bufs == 1 && !mbox_in_ring && m_pad == 64;
+}
+
 __host__ __device__ inline uint32_t ring_bytes_of(int tile_n, int m_pad, int stages, int kb_per_stage)
 {
     return (uint32_t)stages * (uint32_t)kb_per_stage * (w_block_bytes(tile_n) + (uint32_t)m_pad * 128u);
@@ -140,8 +156,12 @@ __host__ __device__ inline SmemLayout make_smem_layout(int tile_n, int m_pad, in
     off += (uint32_t)stages * (uint32_t)kb_per_stage * w_block_bytes(tile_n);
     L.a = off;                                            // [stages][kb_per_stage][m_pad][64 k]; m_pad*128 % 1024 == 0
     off += (uint32_t)stages * (uint32_t)kb_per_stage * (uint32_t)m_pad * 128u;
-    const uint32_t mbox_bytes = (uint32_t)bufs * (uint32_t)(split_k - 1) * (uint32_t)tile_n * (uint32_t)m_pad * 4u;
-    const uint32_t out_bytes = (uint32_t)bufs * (uint32_t)m_pad * (uint32_t)tile_n * 2u;
+    // Reduce-scatter (reduce_scatter_of): each rank receives and stores half of
+    // the tile's m_pad rows.
+    const uint32_t rows = reduce_scatter_of(m_pad, split_k, bufs, mbox_in_ring) ? (uint32_t)m_pad / 2u
+                                                                                 : (uint32_t)m_pad;
+    const uint32_t mbox_bytes = (uint32_t)bufs * (uint32_t)(split_k - 1) * (uint32_t)tile_n * rows * 4u;
+    const uint32_t out_bytes = (uint32_t)bufs * rows * (uint32_t)tile_n * 2u;
     if (mbox_in_ring) {
         L.mailbox = L.w;                                  // [split_k-1] slots of tile_n x m_pad fp32 (*)
         L.out = L.w + mbox_bytes;                         // [m_pad][tile_n] bf16 staging for C
@@ -369,21 +389,25 @@ __device__ __forceinline__ void probe_before_dealloc(const KernelParams &p, int 
 // is tile_n / 8 chunks; a partial last tile stores only the chunks below N),
 // element stores otherwise (rows of C are then not 16-byte aligned).
 template <int TILE_N>
-__device__ __forceinline__ void store_tile(const KernelParams &p, const __nv_bfloat16 *stage_out, int n0, int etid)
+__device__ __forceinline__ void store_tile(const KernelParams &p, const __nv_bfloat16 *stage_out, int n0, int etid,
+                                           int m0 = 0, int m1 = -1)
 {
+    // Rows [m0, min(m1, M)) of C from staging rows [0, m1 - m0).
+    const int rows = (m1 < 0 || m1 > p.M ? p.M : m1) - m0;
+    __nv_bfloat16 *C = p.C + (size_t)m0 * p.N;
     if ((p.N & 7) == 0) {
-        for (int c = etid; c < p.M * (TILE_N / 8); c += kEpilogueThreads) {
+        for (int c = etid; c < rows * (TILE_N / 8); c += kEpilogueThreads) {
             const int m = c / (TILE_N / 8), ch = c % (TILE_N / 8);   // 16-byte chunk ch of row m
             if (n0 + ch * 8 < p.N) {
                 const uint4 v = *reinterpret_cast<const uint4 *>(stage_out + m * TILE_N + ch * 8);
-                *reinterpret_cast<uint4 *>(p.C + (size_t)m * p.N + n0 + ch * 8) = v;
+                *reinterpret_cast<uint4 *>(C + (size_t)m * p.N + n0 + ch * 8) = v;
             }
         }
     } else {
-        for (int e = etid; e < p.M * TILE_N; e += kEpilogueThreads) {
+        for (int e = etid; e < rows * TILE_N; e += kEpilogueThreads) {
             const int m = e / TILE_N, col = e % TILE_N;
             if (n0 + col < p.N)
-                p.C[(size_t)m * p.N + n0 + col] = stage_out[m * TILE_N + col];
+                C[(size_t)m * p.N + n0 + col] = stage_out[m * TILE_N + col];
         }
     }
 }
@@ -406,6 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int kbs = p.kb_per_stage;
     const bool alias = SPLIT_K > 1 && p.mbox_in_ring != 0;       // mailbox + staging in the drained ring
+    constexpr bool kRsCapable = reduce_scatter_of(M_PAD, SPLIT_K, 1, false);
+    const bool rs = kRsCapable && !alias;                         // reduce-scatter epilogue
     const SmemLayout L = make_smem_layout(TILE_N, M_PAD, SPLIT_K, p.stages, kbs, 1, alias);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int stages = p.stages;
@@ -435,10 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // while the later chunks are still arriving.
     const uint32_t bar_reduce3 = bar_acc + 40u;
     const uint32_t bar_reduce4 = bar_acc + 48u;
-    // m_pad 64 splits each slot's float4 columns into two halves with a
-    // barrier each, so the owner reduces and stages the first half while the
-    // second is still arriving (GB300, M64 N6144 K4096: 11.55 -> 11.31 us; at
-    // m_pad 32 the 8 KiB slot gains nothing: 10.09 -> 10.14 us).
+    // m_pad 64 with the mailbox in the ring, or with split_k above 2, splits
+    // each slot's float4 columns into two halves with a barrier each, so the
+    // owner reduces and stages the first half while the second is still
+    // arriving (GB300, M64 N6144 K4096: 11.55 -> 11.31 us; at m_pad 32 the 8
+    // KiB slot gains nothing: 10.09 -> 10.14 us).
     constexpr bool kTwoPhase = SPLIT_K > 1 && M_PAD == 64;
     constexpr int kHalf4 = M_PAD / 8;                              // float4 columns in the first half
     const uint32_t tmem_slot = sbase + L.tmem_slot;
@@ -457,7 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar_reduce3, 1);
         ptx::mbar_init(bar_reduce4, 1);
         *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot + kTicketOffset) = 0u;
-        if (SPLIT_K > 1 && rank == 0) {   // arm the mailbox: every peer sends one full partial tile
+        if (rs) {                          // arm this rank's half: the other rank sends half a tile
+            ptx::mbar_arrive_expect_tx(bar_reduce, kSlotBytes / 2);
+        } else if (SPLIT_K > 1 && rank == 0) {   // arm the mailbox: every peer sends one full partial tile
             if (M_PAD == 128) {
                 ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 4);
                 ptx::mbar_arrive_expect_tx(bar_reduce2, (SPLIT_K - 1) * kSlotBytes / 4);
@@ -705,7 +734,64 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             int row;
             const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile
-            if (SPLIT_K > 1 && rank != 0) {
+            if (kRsCapable && rs) {
+                if constexpr (kRsCapable) {
+                    // Reduce-scatter: this rank keeps half `rank` of the m_pad rows.
+                    // It sends its partial of the other half into the other rank's
+                    // mailbox, then (relaxed cluster-scope wait, acquire fence) adds
+                    // the other rank's partial of its own half: with two ranks the
+                    // rank-ordered sum p0 + p1 is the same value in either operand
+                    // order.  bf16 into staging, then its rows of C.
+                    constexpr int kH4 = M_PAD / 8;                 // float4 columns per half
+                    __nv_bfloat16 *stage_out = reinterpret_cast<__nv_bfloat16 *>(smem + L.out);
+                    const float4 *box = reinterpret_cast<const float4 *>(smem + L.mailbox);
+                    auto keep_half = [&](auto half) {
+                        constexpr int H = decltype(half)::value, X = 1 - H;
+                        if (ok && valid && !p.drop_mailbox) {
+                            const uint32_t dst = ptx::mapa_shared(sbase + L.mailbox + 16u * (uint32_t)row, (uint32_t)X);
+                            const uint32_t rbar = ptx::mapa_shared(bar_reduce, (uint32_t)X);
+#pragma unroll
+                            for (int i = 0; i < kH4; ++i)
+                                ptx::st_async_v4(dst + 16u * kTileN * i, rbar, acc[4 * (X * kH4 + i)],
+                                                 acc[4 * (X * kH4 + i) + 1], acc[4 * (X * kH4 + i) + 2],
+                                                 acc[4 * (X * kH4 + i) + 3]);
+                        }
+                        bool okh = ok;
+                        if (!owner_wait_mailbox(p, bar_reduce, 0))
+                            okh = false;
+                        ptx::fence_acquire_shared_cluster();
+                        if (valid) {
+                            if (okh) {
+#pragma unroll
+                                for (int i = 0; i < kH4; ++i) {
+                                    const float4 v = box[i * kTileN + row];
+                                    acc[4 * (H * kH4 + i)] += v.x;
+                                    acc[4 * (H * kH4 + i) + 1] += v.y;
+                                    acc[4 * (H * kH4 + i) + 2] += v.z;
+                                    acc[4 * (H * kH4 + i) + 3] += v.w;
+                                }
+                            }
+#pragma unroll
+                            for (int m = 0; m < M_PAD / 2; ++m)
+                                stage_out[m * kTileN + row] = __float2bfloat16_rn(acc[H * (M_PAD / 2) + m]);
+                            if (p.c_f32 != nullptr) {
+#pragma unroll
+                                for (int m = H * (M_PAD / 2); m < (H + 1) * (M_PAD / 2); ++m)
+                                    if (m < p.M && n0 + row < p.N)
+                                        p.c_f32[(size_t)m * p.N + n0 + row] = acc[m];
+                            }
+                        }
+                        ptx::named_barrier_sync(1, kEpilogueThreads);
+                        store_tile<kTileN>(p, stage_out, n0, etid, H * (M_PAD / 2), (H + 1) * (M_PAD / 2));
+                    };
+                    if (rank == 0)
+                        keep_half(std::integral_constant<int, 0>{});
+                    else
+                        keep_half(std::integral_constant<int, 1>{});
+                    if (p.timeline != nullptr && etid == 0)
+                        p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
+                }
+            } else if (SPLIT_K > 1 && rank != 0) {
                 // Non-owner: publish the partial tile into rank 0's mailbox slot (rank - 1).
                 const bool open = peer_wait_mailbox_open(p, alias, bar_open);
                 if (ok && open && valid && !p.drop_mailbox) {

@@ -230,8 +230,10 @@ def test_a_dropped_mailbox_times_out_and_the_context_survives():
 
 @pytest.mark.parametrize("M,split_k", [(64, 2), (64, 4), (32, 2)])
 def test_a_dropped_two_phase_mailbox_times_out(M, split_k):
-    # m_pad 64 waits on two mailbox halves (m_pad 32 on one); every bounded
-    # wait must run out, report the mailbox bit, and leave a working context.
+    # m_pad 64 with split_k 4 waits on two mailbox halves, m_pad 32 on one,
+    # and m_pad 64 with split_k 2 (reduce-scatter) on one per rank, every rank
+    # a receiver; every bounded wait must run out, report the mailbox bit,
+    # and leave a working context.
     N, K = 256, 1024
     A, W = inputs.make_problem(M, N, K, seed=5)
     Ad, Wd = A.to(DEV), W.to(DEV)
@@ -242,6 +244,39 @@ def test_a_dropped_two_phase_mailbox_times_out(M, split_k):
     st, detail = lowm.lowm_gemm_sync_status()
     assert st == lowm.LOWM_ERR_TIMEOUT and detail == (1 << 8), (st, hex(detail))
     check(A, W, split_k)
+
+
+# ---------------------------------------------------------------- reduce-scatter exchange (m_pad 64, split_k 2)
+@pytest.mark.parametrize("M,N,flags", [(33, 6144, 1), (40, 6144, 0), (47, 256, 0), (48, 6144, 1), (63, 200, 0),
+                                       (64, 6144, 0), (64, 6144, 1), (64, 6150, 1), (64, 70, 0), (64, 1, 0)])
+def test_reduce_scatter_rows(M, N, flags):
+    # Each rank keeps half of the 64 padded rows: rank 1's half holds 1..32
+    # real rows, and 64- and 128-column tiles, N tails and both launch flags
+    # take the same exchange.
+    K = 4096
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, 2, flags)
+    assert st == lowm.LOWM_OK and (t["m_pad"], t["split_k"], t["mbox_in_ring"]) == (64, 2, 0)
+    A, W = inputs.make_problem(M, N, K, seed=1400 + M + N)
+    check(A, W, 2, flags=flags)
+
+
+def test_reduce_scatter_is_exact_on_integer_inputs():
+    # Integer operands: both halves bit-exact in bf16 and in the fp32 sums.
+    A, W = inputs.make_problem(64, 6144, 8192, seed=1410, kind="int")
+    check(A, W, 2, exact=True)
+
+
+def test_reduce_scatter_twenty_launches_are_bitwise_identical():
+    M, N, K = 64, 6144, 4096
+    A, W = inputs.make_problem(M, N, K, seed=1420)
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    outs = torch.empty((20, M, N), dtype=torch.bfloat16, device=DEV)
+    for i in range(20):
+        assert lowm.lowm_gemm_bf16_ex(Ad, Wd, outs[i], M, N, K, 2, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT, None) == \
+            lowm.LOWM_OK
+    sync_ok()
+    o = outs.view(torch.int16)
+    assert bool((o == o[0:1]).all())
 
 
 def test_w_before_pdl_wait_flag_keeps_the_chain_correct():

@@ -131,10 +131,11 @@ def test_stalled_second_mma_issuer_with_tmem_hog(M, N, K, split_k):
         check_probes(probes)
 
 
-@pytest.mark.parametrize("stall_rank_mask", [1, 2])
-def test_stalling_only_one_rank(stall_rank_mask):
-    # The pages also stall only the owner or only the non-owner rank.
-    M, N, K, split_k = 4, 6144, 4096, 2
+@pytest.mark.parametrize("M,stall_rank_mask", [(4, 1), (4, 2), (64, 1), (64, 2)])
+def test_stalling_only_one_rank(M, stall_rank_mask):
+    # The pages also stall only the owner or only the non-owner rank.  At M64
+    # (reduce-scatter) each rank is both sender and receiver.
+    N, K, split_k = 6144, 4096, 2
     A, W = inputs.make_problem(M, N, K, seed=77)
     Ad, Wd = A.to(DEV), W.to(DEV)
     ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
@@ -168,12 +169,12 @@ def test_persistent_schedule_under_stress(tile, monkeypatch):
 
 @pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (64, 6144, 4096, 2), (16, 6144, 32768, 4)])
 def test_stress_with_the_w_promise(M, N, K, split_k):
-    # The timed tactics (LOWM_FLAG_W_BEFORE_PDL_WAIT: the deeper rings with the
-    # mailbox in the ring, W requested before the dependency wait) under the
-    # same stall + TMEM hog method.
+    # The timed tactics (LOWM_FLAG_W_BEFORE_PDL_WAIT: the deeper rings, W
+    # requested before the dependency wait; at M4 the mailbox in the ring, at
+    # M64 the reduce-scatter exchange) under the same stall + TMEM hog method.
     flags = lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT
     st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, split_k, flags)
-    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 1
+    assert st == lowm.LOWM_OK and t["mbox_in_ring"] == (0 if M == 64 else 1)
     A, W = inputs.make_problem(M, N, K, seed=1234, kind="int")
     Ad, Wd = A.to(DEV), W.to(DEV)
     ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
