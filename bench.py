@@ -96,7 +96,7 @@ def kernel_sources_sha():
 
 def committed_traffic(workload, tactic):
     """DRAM bytes per launch from the committed ncu summary of this workload, if it
-    was taken on the current device code with the same ring."""
+    was taken on the current device code with the same tile width and ring."""
     path = os.path.join(ROOT, "profiles", "lowm_splitk_kernel_m%d_n%d_k%d.md" % (
         workload["M"], workload["N"], workload["K"]))
     try:
@@ -110,6 +110,8 @@ def committed_traffic(workload, tactic):
         if fields.get("workload") != workload_name(workload):
             return None
         if fields.get("ring") != "%d x %d" % (tactic["kb_per_stage"], tactic["stages"]):
+            return None
+        if fields.get("tile_n") != str(tactic["tile_n"]):
             return None
         return int(fields["dram_bytes_per_launch"])
     except Exception:

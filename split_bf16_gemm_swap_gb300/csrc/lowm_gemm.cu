@@ -170,19 +170,22 @@ struct Ring {
 constexpr int kMaxRingBytes = 160 * 1024;     // W bytes per ring when several CTAs share an SM
 
 Ring choose_ring(int tile_n, int m_pad, int split_k, int kb_total, int ctas, int sms, int bufs, bool alias = false,
-                 bool w_promise = false)
+                 bool deep = false)
 {
     const int per_sm_one_wave = (ctas + std::max(1, sms) - 1) / std::max(1, sms);
     const int per_sm = per_sm_one_wave <= 4 ? std::max(1, per_sm_one_wave) : (split_k == 1 ? 3 : 5);
     const int budget = std::min(kMaxSmemPerCta, kSmemPerSm / per_sm - kSmemReservedPerCta);
-    // One CTA per SM, with the caller's W promise (the first ring of W is
-    // requested before the dependency wait): the ring may take all of the
-    // SM's shared memory (a 128-column M4 N6144 K4096 CTA with a 4 x 3 ring,
-    // 192 KiB of W, measured 8.90 us against 9.57 us with the 4 x 2 ring the
-    // 160 KiB cap allows).  Without the promise the deeper rings measured
-    // slower (4 x 3 11.17 against 4 x 2 10.67 us; M4 N2304 K12288 8 x 3 12.13
-    // against 8 x 2 11.67 us), so the cap stays.
-    const int cap = (per_sm == 1 && w_promise) ? kMaxSmemPerCta : kMaxRingBytes;
+    // One CTA per SM and a deep ring allowed (`deep`: the caller's W promise,
+    // under which the first ring of W is requested before the dependency
+    // wait, or a long stream per CTA): the ring may take all of the SM's
+    // shared memory (a 128-column M4 N6144 K4096 CTA with a 4 x 3 ring, 192
+    // KiB of W, measured 8.90 us against 9.57 us with the 4 x 2 ring the 160
+    // KiB cap allows; without the promise, M4 N2304 K12288 split_k 4 on 128
+    // columns, 768 KiB of W per CTA: 11.50 us against 12.12 us).  Short
+    // streams without the promise measured slower with the deeper rings (4 x 3
+    // 11.17 against 4 x 2 10.67 us; M4 N2304 K12288 on 64 columns 8 x 3 12.13
+    // against 8 x 2 11.67 us), so the cap stays there.
+    const int cap = (per_sm == 1 && deep) ? kMaxSmemPerCta : kMaxRingBytes;
     int force_kbs = env_int("LOWM_KB_PER_STAGE", 0);
     if (force_kbs != 1 && force_kbs != 2 && force_kbs != 4 && force_kbs != 8)
         force_kbs = 0;
@@ -219,32 +222,48 @@ bool shape_ok(int M, int N, int K, int split_k)
 }
 
 // Tile width (the MMA's M), given the split.  128 columns when N is a
-// multiple of 128, the 64-column grid would not fit the GPU at one CTA per SM
-// while the 128-column grid does, and each 128-column CTA streams at most 1
-// MiB of W (a short GEMM, where per-GEMM fixed costs weigh most); 64 columns
-// otherwise.  Measured on GB300 with the one-stage L2 prefetch: one CTA per
-// SM streaming a 128-column tile through a ~160 KiB ring is fastest where the
-// 64-column grid overflows the SMs (N6144 K4096 split_k 2: M4 9.43 us against
-// 10.14 with 64 columns, M32 9.59 against 10.32, M64 10.92, M128 14.08
-// against 15.8), while a 64-column grid that already fits, a grid that
-// overflows at both widths, or a long stream per CTA is faster on 64 columns
-// (M4 N2304 K12288 split_k 4: 9.95 against 11.17 us; M4 N49152 K4096: 59.9
-// against 63.4 us; M16 N6144 K32768: 64.2 us at split_k 4 against 69.2 us on
-// 128 columns at split_k 2).  At m_pad 8 a 128-column tile pads the MMA's N
-// to 16 (zero rows from the TMA unit, no extra HBM bytes).  LOWM_TILE_N = 64
-// / 128 overrides when the shape allows it (tuning).
-constexpr double kShortStreamBytes = 1024.0 * 1024.0;   // W bytes per 128-column CTA
+// multiple of 128, the split is at most 4, and the 128-column grid
+//   - has at least 64 CTAs (enough concurrent streams to fill HBM) and at
+//     most two per SM,
+//   - streams at most 768 KiB of W per CTA or has a CTA on every SM,
+//   - and, at m_pad 64 and above, replaces a 64-column grid that would not
+//     fit one CTA per SM, with split_k 2 or one CTA per SM (the m_pad 64
+//     mailbox of three 128-column partials leaves too small a ring);
+// 64 columns otherwise.  Measured on GB300 with the W promise, 64 -> 128
+// columns: N6144 K4096 split_k 2 M4 10.14 -> 9.43 us (M32 10.32 -> 9.59, M128
+// 15.8 -> 14.08); split_k 4 9.72 -> 9.21; N4096 K4096 split_k 2 7.36 -> 6.79;
+// N2048 K8192 split_k 4 7.62 -> 7.15; N3072 K8192 split_k 4 10.39 -> 8.87;
+// N2304 K12288 split_k 4 9.99 -> 9.76 (M16 10.17 -> 10.04); M16 N6144 K32768
+// split_k 4 64.2 -> 63.0; N6144 K16384 split_k 4 33.45 -> 32.72; M64 N8192
+// K12288 split_k 2 34.36 -> 32.95.  Against: fewer than 64 CTAs (N2304 K12288
+// split_k 2, 36 CTAs: 11.96 -> 15.77), more than two per SM (N49152 K4096:
+// 61.1 -> 67.1), long streams on few CTAs (N8192 K8192 split_k 1, 64 CTAs of
+// 2 MiB: 21.6 -> 25.3; N8192 K4096 split_k 1: 11.1 -> 12.4), split_k 8 (its
+// seven 128-column partials take the owner's cluster link: N2304 13.1 ->
+// 15.0), m_pad 64 at split_k 4 with two CTAs per SM (M64 N6144 K4096 17.4 ->
+// 21.1) and m_pad 64 where the 64-column grid fits (M64 N2304 K12288 split_k
+// 4 12.47 -> 13.84).  At m_pad 8 a 128-column tile pads the MMA's N to 16
+// (zero rows from the TMA unit, no extra HBM bytes).  LOWM_TILE_N = 64 / 128
+// overrides when the shape allows it (tuning).
+constexpr int kMinStreams = 64;                          // CTAs that keep HBM busy
+constexpr double kLongStreamBytes = 768.0 * 1024.0;      // W per 128-column CTA below one CTA per SM
+constexpr double kShortStreamBytes = 512.0 * 1024.0;     // W per CTA the auto split aims at
 
-int choose_tile_n(int N, int K, int split_k, int sms)
+int choose_tile_n(int M, int N, int K, int split_k, int sms)
 {
     const int force = env_int("LOWM_TILE_N", 0);
     if (force == 128 && N >= 128)
         return 128;
     if (force == 64)
         return 64;
-    const long long c64 = (long long)((N + 63) / 64) * split_k, c128 = (long long)((N + 127) / 128) * split_k;
+    if (N % 128 != 0 || split_k > 4)
+        return 64;
+    const long long c64 = (long long)((N + 63) / 64) * split_k, c128 = (long long)(N / 128) * split_k;
     const double per_cta = 2.0 * N * (double)K / (double)c128;
-    return (N % 128 == 0 && c64 > sms && c128 <= sms && per_cta <= kShortStreamBytes) ? 128 : 64;
+    const bool wide_pad = m_pad_of(M) >= 64;
+    const bool ok = c128 >= kMinStreams && c128 <= 2LL * sms && (per_cta <= kLongStreamBytes || c128 >= sms) &&
+                    (!wide_pad || (c64 > sms && (split_k <= 2 || c128 <= sms)));
+    return ok ? 128 : 64;
 }
 
 int m_pad_for(int M, int tile_n)
@@ -287,30 +306,39 @@ bool split_usable(int M, int N, int K, int sk, int sms)
 {
     if (K % (sk * lowm::kBlockK) != 0)
         return false;
-    const int tile_n = choose_tile_n(N, K, sk, sms);
+    const int tile_n = choose_tile_n(M, N, K, sk, sms);
     const int mp = m_pad_for(M, tile_n);
     return kernel_for(tile_n, mp, sk, false) &&
            footprint(tile_n, mp, sk, 2, 1, 1, choose_alias(mp, sk)) <= kMaxSmemPerCta;
 }
 
-// split_k = 0.  A short GEMM (at most 1 MiB of W per 128-column CTA) takes the
-// smallest even split that gives between half and all of the SMs one
-// 128-column CTA each (M4..M128 N6144 K4096: split_k 2, 96 CTAs, 9.4-14.1 us,
-// against 9.9 us at split_k 4 on 192 CTAs); otherwise the smallest even split
-// of 64-column tiles that fills 90 % of the SMs (M4 N2304 K12288: split_k 4 on
-// 144 CTAs, 10.07 us, against 11.08 us at split_k 8), where clusters of 8
-// measured slowest.  The K loop stays non-empty and the mailbox fits.
+// split_k = 0.  With N a multiple of 128: the smallest split on 128-column
+// tiles (by the rule above) with at most 512 KiB of W per CTA (N6144 K4096:
+// split_k 2, 96 CTAs, 8.8 us against 9.2 us at split_k 4; N4096 K4096:
+// split_k 2, 64 CTAs, 6.79 against 7.25 us; N8192 K4096: split_k 2, 11.1
+// against 12.4 us at split_k 1), else the largest such split for a long K (M16
+// N6144 K32768: split_k 4, 192 CTAs, 63.0 us against 67.1 us at split_k 2).
+// Otherwise the smallest split of 64-column tiles that fills 90 % of the SMs
+// (M4 N2304 K12288 on 64 columns: split_k 4 on 144 CTAs, 10.07 us, against
+// 11.08 us at split_k 8), stopping at 4 once that gives 64 CTAs: clusters of
+// 8 measured slowest.  The K loop stays non-empty and the mailbox fits.
 int choose_split_k(int M, int N, int K, int sms)
 {
     if (N % 128 == 0) {
         const int tiles128 = N / 128;
+        int longest = 0;
         for (int sk = 1; sk <= 4; sk *= 2) {
             const long long c = (long long)tiles128 * sk;
-            if (c > sms || !split_usable(M, N, K, sk, sms))
+            if (c > 2LL * sms || !split_usable(M, N, K, sk, sms))
                 break;
-            if (2 * c >= sms && 2.0 * N * (double)K / (double)c <= kShortStreamBytes)
+            if (c < kMinStreams || choose_tile_n(M, N, K, sk, sms) != 128)
+                continue;
+            if (2.0 * N * (double)K / (double)c <= kShortStreamBytes)
                 return sk;
+            longest = sk;
         }
+        if (longest)
+            return longest;
     }
     const int tiles64 = (N + 63) / 64;
     int best = 0;
@@ -318,7 +346,7 @@ int choose_split_k(int M, int N, int K, int sms)
         if (!split_usable(M, N, K, sk, sms))
             break;
         best = sk;
-        if (10LL * tiles64 * sk >= 9LL * sms)
+        if (10LL * tiles64 * sk >= 9LL * sms || (sk == 4 && tiles64 * sk >= kMinStreams))
             break;
     }
     return best;
@@ -437,7 +465,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
         return LOWM_ERR_INVALID_ARGUMENT;
     const int nsm = sms > 0 ? sms : 152;
     const bool w_promise = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) != 0;
-    int tile_n = choose_tile_n(N, K, split_k, nsm);
+    int tile_n = choose_tile_n(M, N, K, split_k, nsm);
     int m_pad = m_pad_for(M, tile_n);
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1); it splits K evenly.
     bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad != 128 &&   // no persistent m_pad 128 instance
@@ -451,15 +479,21 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     // mailbox in the ring when that is fixed, else whichever placement fits
     // the larger W ring (the separate mailbox on a tie: no hand-off needed).
     auto pick = [&]() {
-        // Without the W promise the mailbox shares the ring only where it must
-        // (M64 N6144 K4096 with default flags, before the reduce-scatter
-        // mailbox: 2 x 3 next to the mailbox 12.17 us against 4 x 2 in the
-        // ring 12.36 us).
+        // Deep rings (and the mailbox in the ring, where that deepens it) with
+        // the W promise or a stream of more than 512 KiB of W per CTA.  Short
+        // streams without the promise keep the mailbox next to the ring unless
+        // it must share it (M64 N6144 K4096 with default flags, before the
+        // reduce-scatter mailbox: 2 x 3 next to the mailbox 12.17 us against
+        // 4 x 2 in the ring 12.36 us); long ones gain from it (M16 N6144 K32768
+        // split_k 4 on 128 columns: 2 x 3 in the ring, two CTAs per SM, 61.6
+        // us against 2 x 2 next to the mailbox 63.8 us).
+        const double per_cta_w = 2.0 * N * (double)K / ((double)tiles * split_k);
+        const bool deep = w_promise || per_cta_w > kShortStreamBytes;
         int fa = forced_alias(m_pad, split_k);
-        if (fa < 0 && !w_promise)
+        if (fa < 0 && !deep)
             fa = 0;
         auto one = [&](bool al, Ring &r, int &f) {
-            r = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, al, w_promise);
+            r = choose_ring(tile_n, m_pad, split_k, kbt, tiles * split_k, nsm, 1, al, deep);
             if (stages_override >= 2)
                 r.stages = stages_override;
             f = footprint(tile_n, m_pad, split_k, r.stages, r.kbs, 1, al);
@@ -544,7 +578,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     const int force_wpf = env_int("LOWM_W_PREFETCH", -1);
     if (force_wpf >= 0)
         wpf = std::min(force_wpf, stages);
-    t->w_prefetch_stages = wpf;
+    t->w_prefetch_stages = w_promise ? wpf : 0;      // nothing is requested before the wait without the flag
     // W stages requested into L2 ahead of the newest ring load: one measured
     // fastest for every workload (GB300, interleaved repeats: M4 N6144 K4096
     // split_k 2 10.49 -> 10.15 us, M4 N2304 K12288 split_k 4 10.73 -> 9.95,
@@ -681,7 +715,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     p.num_tiles = t.tiles;
     p.timeout_ns = lowm::kDefaultTimeoutNs;
     p.reduce_timeout_ns = lowm::kDefaultTimeoutNs;
-    p.w_prefetch_stages = (flags & LOWM_FLAG_W_BEFORE_PDL_WAIT) ? (uint32_t)t.w_prefetch_stages : 0u;
+    p.w_prefetch_stages = (uint32_t)t.w_prefetch_stages;   // 0 unless the flag is set
     p.l2_prefetch_stages = (uint32_t)t.l2_prefetch_stages;
     if (dbg) {
         p.stall_warp_mask = dbg->stall_warp_mask;

@@ -75,13 +75,20 @@ def test_default_tactic_for_the_headline_workload(L):
 
 
 @pytest.mark.parametrize("M,N,K,sk,tile", [
-    # 128 columns where the 64-column grid overflows the SMs and the 128-column grid fits with a short stream
+    # GB300, W promise, 64 -> 128 columns (us): 128 columns on 64 to two-per-SM CTAs with short streams
     (4, 6144, 4096, 2, 128), (16, 6144, 4096, 2, 128), (32, 6144, 4096, 2, 128), (64, 6144, 4096, 2, 128),
-    (128, 6144, 4096, 2, 128),
-    (4, 2304, 12288, 4, 64),      # the 64-column grid (144 CTAs) already fits
-    (4, 49152, 4096, 2, 64),      # both widths overflow the SMs
-    (16, 6144, 32768, 4, 64),     # both overflow
-    (16, 6144, 32768, 2, 64),     # fits, but 4 MiB of W per 128-column CTA
+    (128, 6144, 4096, 2, 128),    # 10.14 -> 9.43 at M4
+    (4, 2304, 12288, 4, 128),     # 72 CTAs of 768 KiB: 9.97 -> 9.67
+    (4, 4096, 4096, 2, 128),      # 64 CTAs: 7.36 -> 6.79
+    (4, 6144, 4096, 4, 128),      # 192 CTAs, two per SM: 9.72 -> 9.21
+    (16, 6144, 32768, 4, 128),    # 192 CTAs of 2 MiB, a CTA on every SM: 62.5 -> 61.1
+    (4, 2304, 12288, 2, 64),      # 36 CTAs: 11.96 -> 15.77
+    (4, 2304, 12288, 8, 64),      # split_k 8: 13.1 -> 15.0
+    (4, 49152, 4096, 2, 64),      # four CTAs per SM: 61.1 -> 67.1
+    (4, 8192, 8192, 1, 64),       # 64 CTAs of 2 MiB: 21.6 -> 25.3
+    (16, 6144, 32768, 2, 64),     # 96 CTAs of 4 MiB
+    (64, 6144, 4096, 4, 64),      # m_pad 64, split_k 4, two per SM: 17.4 -> 21.1
+    (64, 2304, 12288, 4, 64),     # m_pad 64 where the 64-column grid fits: 12.47 -> 13.84
     (4, 6152, 4096, 2, 64)])      # N not a multiple of 128
 def test_tile_width_rule(L, M, N, K, sk, tile):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
@@ -90,8 +97,13 @@ def test_tile_width_rule(L, M, N, K, sk, tile):
 
 @pytest.mark.parametrize("M,N,K,sk,tile", [
     (1, 6144, 4096, 2, 128), (64, 6144, 4096, 2, 128), (128, 6144, 4096, 2, 128),   # short GEMMs: 96 CTAs
-    (4, 2304, 12288, 4, 64),      # fills 90 % of the SMs with 64-column tiles (split 8 measured slower)
-    (4, 49152, 4096, 1, 64), (16, 6144, 32768, 2, 64)])
+    (4, 4096, 4096, 2, 128),      # 64 CTAs: 6.79 us against 7.25 at split_k 4
+    (4, 8192, 4096, 2, 128),      # 11.1 us against 12.4 at split_k 1 (64 CTAs of 1 MiB)
+    (4, 2304, 12288, 4, 128),     # 72 CTAs: 9.67 us against 9.97 on 144 64-column CTAs
+    (4, 2048, 8192, 4, 128),      # 7.13 us against 12.2 at split_k 8
+    (16, 6144, 32768, 4, 128),    # long K: 61.1 us against 67.1 at split_k 2
+    (4, 1024, 16384, 4, 64),      # too few 128-column CTAs; 8.62 us against 14.6 at split_k 8
+    (4, 49152, 4096, 1, 64)])
 def test_auto_split_is_the_measured_best(L, M, N, K, sk, tile):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, 0)
     assert st == lowm.LOWM_OK and (t["split_k"], t["tile_n"]) == (sk, tile)
@@ -119,9 +131,9 @@ def test_cluster_counts_for_the_workloads(L, M, N, K, sk):
     (4, 6144, 4096, 2, 128, 4, 3, 1),       # 8.90 us; 4 x 2 next to the mailbox 9.53 us
     (64, 6144, 4096, 2, 128, 4, 2, 0),      # reduce-scatter mailbox next to the ring 9.88 us; in the ring 10.66 us
     (128, 6144, 4096, 2, 128, 2, 3, 1),     # 13.2 us; 2 x 2 next to the mailbox 16.4 us
-    (4, 2304, 12288, 4, 64, 8, 3, 0),       # one CTA per SM: 9.98 us (whole ring before the PDL wait); 8 x 2 10.06 us
+    (4, 2304, 12288, 4, 128, 4, 3, 1),      # 9.67 us; 4 x 2 next to the mailbox 11.06, 2 x 5 12.44 us
     (4, 49152, 4096, 2, 64, 2, 2, 0), (4, 49152, 4096, 1, 64, 4, 2, 0),
-    (16, 6144, 32768, 4, 64, 2, 3, 1)])     # 64.1 us; 2 x 2 next to the mailbox 63.9 us (within noise)
+    (16, 6144, 32768, 4, 128, 2, 3, 1)])    # 61.1 us, two CTAs per SM; 2 x 2 next to the mailbox 63.2, 4 x 3 64.8 us
 def test_ring_matches_the_measured_best(L, M, N, K, sk, tile, kbs, stages, alias):
     # the benchmark's launches carry the W-before-PDL promise
     st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
@@ -133,7 +145,8 @@ def test_ring_matches_the_measured_best(L, M, N, K, sk, tile, kbs, stages, alias
     # without the W promise (default flags, GB300 sweep): the rings within 160 KiB of W
     (4, 6144, 4096, 2, 128, 4, 2, 0),       # 10.67 us; 4 x 3 in the ring 11.17 us
     (64, 6144, 4096, 2, 128, 4, 2, 0),      # reduce-scatter 11.43 us; 2 x 3 owner-only 12.15 us
-    (4, 2304, 12288, 4, 64, 8, 2, 0)])      # 11.67 us; 8 x 3 12.13 us
+    (4, 2304, 12288, 4, 128, 4, 3, 1),      # 768 KiB per CTA: 11.50 us; 4 x 2 next to the mailbox 12.12 us
+    (16, 6144, 32768, 4, 128, 2, 3, 1)])    # 61.6 us; 2 x 2 next to the mailbox 63.8 us
 def test_ring_without_the_w_promise(L, M, N, K, sk, tile, kbs, stages, alias):
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, sk)
     assert st == lowm.LOWM_OK
@@ -201,7 +214,7 @@ def test_any_n_is_tiled_with_a_partial_last_tile(L, M, N, K, sk):
     # one W stage ahead of the PDL wait for three-stage 64-column rings on a grid that overflows
     # the SMs, the whole ring otherwise (GB300 sweeps)
     (4, 6152, 4096, 2, 1), (4, 6144, 4096, 2, 3), (8, 6144, 4096, 2, 3), (4, 2304, 12288, 4, 3), (4, 49152, 4096, 2, 2),
-    (16, 6144, 32768, 4, 1), (64, 6144, 4096, 2, 2), (32, 6144, 4096, 2, 2)])
+    (16, 6144, 32768, 4, 3), (64, 6144, 4096, 2, 2), (32, 6144, 4096, 2, 2)])
 def test_two_mma_issuers_and_prefetch_depth(L, M, N, K, sk, wpf):
     st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     assert st == lowm.LOWM_OK and t["mma_issuers"] == 2 and t["persistent"] == 0
@@ -209,12 +222,21 @@ def test_two_mma_issuers_and_prefetch_depth(L, M, N, K, sk, wpf):
 
 
 def test_prefetch_depth_override_is_capped_by_the_ring(L, monkeypatch):
+    flags = lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT
     monkeypatch.setenv("LOWM_W_PREFETCH", "9")
-    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, flags)
     assert st == lowm.LOWM_OK and t["w_prefetch_stages"] == t["stages"]
     monkeypatch.setenv("LOWM_W_PREFETCH", "0")
-    st, t = lowm.lowm_gemm_query_tactic(4, 6144, 4096, 2)
+    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, flags)
     assert st == lowm.LOWM_OK and t["w_prefetch_stages"] == 0
+
+
+def test_nothing_is_prefetched_before_the_wait_without_the_flag(L):
+    # Without LOWM_FLAG_W_BEFORE_PDL_WAIT the kernel requests nothing before
+    # griddepcontrol.wait, and the tactic says so.
+    for shape in [(4, 6144, 4096, 2), (4, 2304, 12288, 4), (4, 49152, 4096, 2)]:
+        st, t = lowm.lowm_gemm_query_tactic(*shape)
+        assert st == lowm.LOWM_OK and t["w_prefetch_stages"] == 0
 
 
 def test_persistent_schedule_has_one_issuer(L, monkeypatch):

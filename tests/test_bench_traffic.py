@@ -38,10 +38,17 @@ def test_traffic_is_withheld_when_the_ring_differs():
     assert bench.committed_traffic(bench.WORKLOAD, t) is None
 
 
+def test_traffic_is_withheld_when_the_tile_width_differs():
+    t = dict(tactic(bench.WORKLOAD))
+    t["tile_n"] = 64 if t["tile_n"] == 128 else 128
+    assert bench.committed_traffic(bench.WORKLOAD, t) is None
+
+
 def test_traffic_is_withheld_when_the_device_code_changed(monkeypatch):
     monkeypatch.setattr(bench, "kernel_sources_sha", lambda: "0000000000000000")
     assert bench.committed_traffic(bench.WORKLOAD, tactic(bench.WORKLOAD)) is None
 
 
 def test_traffic_is_withheld_for_a_workload_without_a_summary():
-    assert bench.committed_traffic(dict(M=3, N=640, K=1024, split_k=2), {"kb_per_stage": 4, "stages": 2}) is None
+    assert bench.committed_traffic(dict(M=3, N=640, K=1024, split_k=2),
+                                   {"kb_per_stage": 4, "stages": 2, "tile_n": 64}) is None

@@ -322,7 +322,7 @@ def test_every_prefetch_depth_gives_the_same_bits(prefetch, monkeypatch):
     c1 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
     assert lowm.lowm_gemm_bf16(Ad, Wd, c0, M, N, K, split_k, None) == lowm.LOWM_OK
     monkeypatch.setenv("LOWM_W_PREFETCH", prefetch)
-    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, split_k, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     assert t["w_prefetch_stages"] == min(int(prefetch), t["stages"])
     for _ in range(3):
         assert lowm.lowm_gemm_bf16_ex(Ad, Wd, c1, M, N, K, split_k, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT, None) \
