@@ -813,6 +813,22 @@ def test_workloads_with_the_w_promise(M, N, K, split_k, kind):
     assert np.array_equal(C0, C1)
 
 
+@pytest.mark.parametrize("M,N,K,tile,split_k", [
+    (4, 4096, 4096, 128, 2), (4, 2048, 8192, 128, 4), (4, 1024, 16384, 64, 4), (4, 8192, 4096, 128, 2),
+    (16, 6144, 16384, 128, 4), (64, 12288, 8192, 128, 2), (4, 1536, 8192, 64, 4)])
+def test_auto_tactics_of_the_tile_sweep(M, N, K, tile, split_k):
+    # The tactics the 128-column rule and the auto split pick across shapes
+    # (64 to two-per-SM CTAs, 512 KiB of W per CTA, long K), with and without
+    # the W promise, against the oracle.
+    for flags in (0, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT):
+        st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, 0, flags)
+        assert st == lowm.LOWM_OK and (t["tile_n"], t["split_k"]) == (tile, split_k)
+    A, W = inputs.make_problem(M, N, K, seed=1900 + M + N // 64)
+    C1 = check(A, W, 0, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    C0, _ = run_gpu(A, W, 0, want_f32=False)
+    assert np.array_equal(C0, C1)
+
+
 def test_pdl_chain_with_the_deep_ring_and_w_promise():
     # C of each GEMM is the next GEMM's A (K = N = 6144), launched back to back
     # with the W promise: the 128-column tactic with the 4 x 3 ring and the
