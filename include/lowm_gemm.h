@@ -114,6 +114,13 @@ typedef enum {
  *                ring load, so that one more stage of W is in flight than the
  *                ring's shared memory holds (0: none; the persistent kernel
  *                uses none)
+ *   l2_before_wait_stages  without LOWM_FLAG_W_BEFORE_PDL_WAIT: stages of W
+ *                requested into L2 (not into shared memory) before the
+ *                programmatic-dependency wait.  A kernel that runs before
+ *                this one and writes W writes through L2, so the later ring
+ *                loads still read the current W; no promise is needed.  0
+ *                with the flag (the ring itself is then requested early) and
+ *                for the persistent kernel.
  * The pages' shipped tactic reads as (tile_n 64, m_pad 8, split_k 2, stages 10)
  * ("Fix two synchronization gaps ...", Hardware verification).
  */
@@ -123,6 +130,7 @@ typedef struct {
     int persistent, tiles_per_cluster, kb_per_stage;
     int mma_issuers, w_prefetch_stages;
     int mbox_in_ring, l2_prefetch_stages;
+    int l2_before_wait_stages;
 } lowm_tactic_t;
 
 /*

@@ -590,6 +590,21 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     if (force_l2pf >= 0 && !persistent)
         l2pf = force_l2pf;
     t->l2_prefetch_stages = l2pf;
+    // Without the W promise nothing may land in shared memory before the
+    // dependency wait, but W may be requested into L2 (every SM's stores
+    // land there, so the line a later ring load reads is the current one):
+    // one stage for a short stream, the whole ring for more than 512 KiB of
+    // W per CTA (GB300, default flags, 0 -> 1 stage: M4 N6144 K4096 10.60 ->
+    // 10.25 us, M64 11.37 -> 11.03; 0 -> 3: M4 N2304 K12288 split_k 4 11.69 ->
+    // 11.25, M16 N6144 K32768 split_k 4 63.41 -> 62.76; two or more stages
+    // lost on the short streams: 10.71 us at two).  LOWM_L2_BEFORE_WAIT
+    // overrides (tuning).
+    const double w_per_cta = 2.0 * N * (double)K / ((double)t->ctas);
+    int l2bw = (w_promise || persistent) ? 0 : (w_per_cta > kShortStreamBytes ? t->stages : 1);
+    const int force_l2bw = env_int("LOWM_L2_BEFORE_WAIT", -1);
+    if (force_l2bw >= 0 && !w_promise && !persistent)
+        l2bw = force_l2bw;
+    t->l2_before_wait_stages = l2bw;
     return LOWM_OK;
 }
 
@@ -717,6 +732,7 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     p.reduce_timeout_ns = lowm::kDefaultTimeoutNs;
     p.w_prefetch_stages = (uint32_t)t.w_prefetch_stages;   // 0 unless the flag is set
     p.l2_prefetch_stages = (uint32_t)t.l2_prefetch_stages;
+    p.l2_before_wait_stages = (uint32_t)t.l2_before_wait_stages;
     if (dbg) {
         p.stall_warp_mask = dbg->stall_warp_mask;
         p.stall_rank_mask = dbg->stall_rank_mask;

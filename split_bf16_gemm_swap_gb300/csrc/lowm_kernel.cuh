@@ -108,6 +108,8 @@ struct KernelParams {
     uint32_t w_prefetch_stages;   // stages of W requested before the programmatic-dependency wait
                                   // (0 unless the caller promised the preceding kernel does not write W)
     uint32_t l2_prefetch_stages;  // W stages requested into L2 ahead of the newest ring load (0: none)
+    uint32_t l2_before_wait_stages;   // W stages requested into L2 before the programmatic-dependency
+                                      // wait (0 when the W promise requests the ring itself early)
     unsigned long long *probes;     // [kProbeWords * ctas], see lowm_debug_opts_t
     float *c_f32;
     unsigned long long *timeline;   // [4 * ctas]: prologue end, first / last full stage, epilogue end
@@ -553,6 +555,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(sbase + L.w + (uint32_t)i * w_stage_bytes, &tmap_w, 0, n0, kb0 + i * kbs,
                                  bar_full + 8u * i, pol_w);
             }
+            // Without the W promise, the first stages of W go to L2 (not to
+            // shared memory) before the wait: L2 is where every SM's stores
+            // land, so a line requested early is still the current one after
+            // the wait, and the ring loads behind the wait then hit L2.
+            const int l2w = pre > 0 ? 0 : (n_stages < (int)p.l2_before_wait_stages ? n_stages : (int)p.l2_before_wait_stages);
+            for (int i = 0; i < l2w; ++i)
+                ptx::tma_prefetch_3d(&tmap_w, 0, n0, kb0 + i * kbs);
             ptx::griddep_wait();          // A (and C) may belong to the previous kernel in the stream
             for (int i = 0; i < pre; ++i)
                 ptx::tma_load_3d(sbase + L.a + (uint32_t)i * a_stage_bytes, &tmap_a, 0, 0, kb0 + i * kbs,
@@ -563,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (Requested before the dependency wait instead, they slowed the
             // preceding kernel's tail: 9.53 -> 11.0 us at M4 N6144 K4096.)
             const int l2pf = (int)p.l2_prefetch_stages;
-            int next_pf = pre;
+            int next_pf = pre > l2w ? pre : l2w;
             while (next_pf < n_stages && next_pf < pre + l2pf) {
                 ptx::tma_prefetch_3d(&tmap_w, 0, n0, kb0 + next_pf * kbs);
                 ++next_pf;

@@ -43,7 +43,7 @@ class lowm_tactic_t(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in
                 ("tile_n", "m_pad", "split_k", "stages", "block_k", "tiles", "num_clusters", "ctas", "smem_bytes",
                  "pdl", "persistent", "tiles_per_cluster", "kb_per_stage", "mma_issuers", "w_prefetch_stages",
-                 "mbox_in_ring", "l2_prefetch_stages")]
+                 "mbox_in_ring", "l2_prefetch_stages", "l2_before_wait_stages")]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -239,6 +239,17 @@ def test_nothing_is_prefetched_before_the_wait_without_the_flag(L):
         assert st == lowm.LOWM_OK and t["w_prefetch_stages"] == 0
 
 
+@pytest.mark.parametrize("M,N,K,sk,flags,l2bw", [
+    # GB300, default flags: one stage of W into L2 before the wait for short streams (M4 N6144 K4096 10.60 ->
+    # 10.25 us), the whole ring for long ones (M4 N2304 K12288 split_k 4 11.69 -> 11.25 us); none with the
+    # W promise, which requests the ring itself before the wait
+    (4, 6144, 4096, 2, 0, 1), (64, 6144, 4096, 0, 0, 1), (4, 2304, 12288, 4, 0, 3), (16, 6144, 32768, 4, 0, 3),
+    (4, 6144, 4096, 2, 1, 0), (4, 2304, 12288, 4, 1, 0)])
+def test_l2_requests_before_the_wait(L, M, N, K, sk, flags, l2bw):
+    st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, flags)
+    assert st == lowm.LOWM_OK and t["l2_before_wait_stages"] == l2bw
+
+
 def test_persistent_schedule_has_one_issuer(L, monkeypatch):
     monkeypatch.setenv("LOWM_PERSISTENT", "1")
     st, t = lowm.lowm_gemm_query_tactic(4, 49152, 4096, 2)

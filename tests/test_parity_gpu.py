@@ -298,6 +298,34 @@ def test_w_before_pdl_wait_flag_keeps_the_chain_correct():
         assert torch.equal(ref.view(torch.int16), Cs[i + 1].view(torch.int16)), "link %d" % i
 
 
+@pytest.mark.parametrize("M1,N1,K1,N2,K2", [(128, 4096, 2048, 128, 4096), (128, 6144, 1024, 768, 1024),
+                                              (64, 6144, 4096, 3072, 128)])
+def test_w_written_by_the_previous_gemm_without_the_promise(M1, N1, K1, N2, K2):
+    # Without the W promise a CTA requests the first stages of W into L2
+    # before the dependency wait.  Here W of the second GEMM is the first
+    # GEMM's output, launched back to back with no synchronization between
+    # them, so those requests can run while the first GEMM still writes W:
+    # the second GEMM must read W as the first one left it (a separate launch
+    # after a synchronization gives the same bits, and the oracle agrees).
+    st, t = lowm.lowm_gemm_query_tactic(4, N2, K2, 0)
+    assert st == lowm.LOWM_OK and t["l2_before_wait_stages"] >= 1 and t["w_prefetch_stages"] == 0
+    A1, W1 = inputs.make_problem(M1, N1, K1, seed=71)
+    A2, _ = inputs.make_problem(4, N2, K2, seed=72)
+    A1d, W1d, A2d = A1.to(DEV), W1.to(DEV), A2.to(DEV)
+    for rep in range(3):
+        C1 = torch.full((M1, N1), float("nan"), dtype=torch.bfloat16, device=DEV)
+        C2 = torch.empty((4, N2), dtype=torch.bfloat16, device=DEV)
+        assert lowm.lowm_gemm_bf16(A1d, W1d, C1, M1, N1, K1, 0, None) == lowm.LOWM_OK
+        assert lowm.lowm_gemm_bf16(A2d, C1.view(N2, K2), C2, 4, N2, K2, 0, None) == lowm.LOWM_OK
+        sync_ok()
+        ref = torch.empty((4, N2), dtype=torch.bfloat16, device=DEV)
+        assert lowm.lowm_gemm_bf16(A2d, C1.view(N2, K2), ref, 4, N2, K2, 0, None) == lowm.LOWM_OK
+        sync_ok()
+        assert torch.equal(ref.view(torch.int16), C2.view(torch.int16)), "repeat %d" % rep
+    C = check(A2, C1.view(N2, K2).cpu(), 0)                # the synchronized launch meets the parity bar
+    assert np.array_equal(C, inputs.bits(C2.cpu()))
+
+
 @pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (4, 49152, 4096, 2), (64, 192, 1024, 8),
                                            (3, 64, 64, 1)])
 def test_w_before_pdl_wait_flag_gives_the_same_bits(M, N, K, split_k):
