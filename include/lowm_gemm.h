@@ -59,9 +59,11 @@ typedef enum {
  * A tactic: how one GEMM is tiled and launched.
  *   tile_n       output columns per CTA; the MMA's M dimension (swap-AB: N is
  *                mapped onto the tensor core's M, the tiny M onto its N): 128
- *                when N % 128 == 0, the 64-column grid would not fit the GPU
- *                at one CTA per SM while the 128-column grid does, and each
- *                128-column CTA streams at most 1 MiB of W; else 64
+ *                when N % 128 == 0, split_k <= 4 and the 128-column grid has
+ *                64 CTAs to two per SM, each streaming at most 768 KiB of W
+ *                unless every SM gets one (at m_pad >= 64 also: the
+ *                64-column grid would not fit one CTA per SM, and split_k 2
+ *                or one CTA per SM); else 64
  *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64 or 128;
  *                at least 16 for 128-column tiles); rows M..m_pad-1 are
  *                zero-filled by the TMA unit and never stored
@@ -87,7 +89,8 @@ typedef enum {
  *                copy of W and one of A (the largest of 8, 4, 2, 1 that
  *                divides the rank's block count and whose two-stage ring
  *                fits the per-SM shared-memory budget, and 160 KiB of W
- *                unless one CTA per SM runs with the W promise): a copy has
+ *                unless one CTA per SM runs with the W promise or streams
+ *                more than 512 KiB of W): a copy has
  *                a fixed per-CTA cost, so larger copies are what let one CTA
  *                stream its share of HBM
  *   mma_issuers  threads issuing tcgen05.mma per CTA: 2 for the one-tile
@@ -194,7 +197,9 @@ lowm_status_t lowm_gemm_query_tactic(int M, int N, int K, int split_k, lowm_tact
  * bits are rejected with LOWM_ERR_INVALID_ARGUMENT).  The choice depends on
  * the W promise: with LOWM_FLAG_W_BEFORE_PDL_WAIT and one CTA per SM the ring
  * may fill the SM's shared memory (its first stages are requested before the
- * dependency wait), without it the ring holds at most 160 KiB of W.
+ * dependency wait); without it the ring holds at most 160 KiB of W unless a
+ * CTA streams more than 512 KiB of W, and the first stages of W are
+ * requested into L2 only (l2_before_wait_stages).
  * lowm_gemm_query_tactic is this call with flags 0.
  */
 lowm_status_t lowm_gemm_query_tactic_ex(int M, int N, int K, int split_k, unsigned int flags, lowm_tactic_t *out);

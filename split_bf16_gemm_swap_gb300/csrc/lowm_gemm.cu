@@ -156,8 +156,8 @@ bool kbs_tiles_k(int kbs, int kb_total, int split_k)
 //     gain nothing (W bytes: the A tiles in the ring come from L2; at m_pad
 //     128 an A block is twice a 64-column W block, and counting it would cap
 //     that ring at 2 x 2 blocks where 4 x 2 measured 15.8 against 17.1 us at
-//     M128 N6144 K4096); with one CTA per SM and the W promise the ring may
-//     fill the SM (below).
+//     M128 N6144 K4096); with one CTA per SM and the W promise, or a long
+//     stream per CTA, the ring may fill the SM (below).
 // Hence: budget shared memory for ceil(ctas / sms) CTAs per SM when that is at
 // most 4 (the whole grid resident at once), else for 3 (split_k 1) or 5; take
 // the most blocks per copy (8, 4, 2, 1, tiling K) whose 2-stage ring fits,
