@@ -402,3 +402,31 @@ def test_split3_defaults_to_the_mailbox_in_the_ring(L, monkeypatch):
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0
     st, t = lowm.lowm_gemm_query_tactic(4, 640, 64 * 9, 1)
     assert st == lowm.LOWM_OK and t["mbox_in_ring"] == 0          # no mailbox at split_k 1
+
+
+def test_every_tactic_of_a_shape_grid_is_launchable(L):
+    # Over a grid of shapes, splits and both launch flags, every accepted
+    # tactic fits the SM, tiles K in whole stages and reports consistent
+    # counts; the host refuses exactly the documented rest (fewer K blocks
+    # than ranks, M above 64 with split_k 8) before any launch.
+    for M in (1, 3, 4, 8, 16, 17, 32, 33, 64, 65, 96, 128):
+        for N in (1, 63, 64, 200, 1024, 2304, 4096, 6144, 6152, 49152):
+            for K in (64, 1024, 4096, 12288, 32768):
+                for sk in (0, 1, 2, 3, 4, 8):
+                    for flags in (0, lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT):
+                        st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, sk, flags)
+                        refuse = K // 64 < max(sk, 1) or (M > 64 and sk == 8)
+                        assert (st == lowm.LOWM_ERR_UNSUPPORTED_SHAPE) == refuse, (M, N, K, sk, flags, st)
+                        if refuse:
+                            continue
+                        where = (M, N, K, sk, flags, t)
+                        assert t["smem_bytes"] <= 232448 and t["stages"] >= 2, where
+                        assert (K // 64) % t["kb_per_stage"] == 0 and K // (64 * t["kb_per_stage"]) >= t["split_k"], where
+                        assert t["tile_n"] in (64, 128) and (t["tile_n"] == 64 or N % 128 == 0), where
+                        assert t["m_pad"] >= M and t["tiles"] == -(-N // t["tile_n"]), where
+                        assert t["ctas"] == t["num_clusters"] * t["split_k"] and (sk == 0 or t["split_k"] == sk), where
+                        assert 0 <= t["w_prefetch_stages"] <= t["stages"], where
+                        if flags:
+                            assert t["l2_before_wait_stages"] == 0, where
+                        else:
+                            assert t["w_prefetch_stages"] == 0 and 0 <= t["l2_before_wait_stages"] <= t["stages"], where
