@@ -64,7 +64,7 @@ typedef enum {
  *                unless every SM gets one (at m_pad >= 64 also: the
  *                64-column grid would not fit one CTA per SM, and split_k 2
  *                or one CTA per SM); else 64
- *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64 or 128;
+ *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64, 96 or 128;
  *                at least 16 for 128-column tiles); rows M..m_pad-1 are
  *                zero-filled by the TMA unit and never stored
  *   split_k      CTAs per cluster along K (1, 2, 3, 4 or 8).  K is cut into
@@ -140,8 +140,9 @@ typedef struct {
  * C = A . W^T on `stream`: the low-M split-K GEMM of the PR page
  * (Description; the launch shape of Hardware verification: clusters of
  * split_k CTAs along the output columns, programmatic dependent launch on).
- *   M        1..128 (M > 64 pads to m_pad 128; those shapes run split_k 1, 2,
- *            3 or 4 with 64-column tiles, 1, 2 or 3 with 128-column tiles)
+ *   M        1..128 (M 65..96 pads to m_pad 96, M 97..128 to 128; those
+ *            shapes run split_k 1, 2, 3 or 4 with 64-column tiles, 1, 2 or 3
+ *            with 128-column tiles)
  *   N        any positive value; when N is not a multiple of tile_n the last
  *            tile is partial (the TMA unit zero-fills W rows >= N and the
  *            epilogue stores only columns < N; 16-byte stores when N % 8 == 0,

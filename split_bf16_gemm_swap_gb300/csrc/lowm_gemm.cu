@@ -126,7 +126,7 @@ int env_int(const char *name, int dflt)
 
 int m_pad_of(int M)
 {
-    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 96 ? 96 : 128;
 }
 
 int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs, bool alias = false)
@@ -273,7 +273,7 @@ int m_pad_for(int M, int tile_n)
 }
 
 // The split-K mailbox shares the drained ring (see make_smem_layout) for
-// split_k 3 and for m_pad 128, whose 32-64 KiB slots would otherwise take the
+// split_k 3 and for m_pad 96 and 128, whose 24-64 KiB slots would otherwise take the
 // ring's room (M128 N6144 K4096 split_k 2 on 128-column tiles: 14.4 us
 // against 16.4 us with the mailbox next to the ring), and otherwise whenever
 // sharing lets the ring hold more W (make_tactic compares both layouts; M4
@@ -290,7 +290,7 @@ int forced_alias(int m_pad, int split_k)
     const int force = env_int("LOWM_MBOX_IN_RING", -1);
     if (force == 0 || force == 1)
         return force;
-    return (split_k == 3 || m_pad == 128) ? 1 : -1;
+    return (split_k == 3 || m_pad > 64) ? 1 : -1;
 }
 
 bool choose_alias(int m_pad, int split_k)
@@ -359,6 +359,8 @@ KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent)
         return nullptr;                                 // the persistent schedule splits K evenly (1, 2, 4, 8)
     if (m_pad == 128)
         return persistent ? nullptr : lowm::kernel_mpad128(tile_n, sk);
+    if (m_pad == 96)
+        return persistent ? nullptr : lowm::kernel_mpad96(tile_n, sk);
     if (tile_n == 64)
         return lowm::kernel_tile64(m_pad, sk, persistent);
     if (tile_n == 128)
@@ -468,7 +470,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     int tile_n = choose_tile_n(M, N, K, split_k, nsm);
     int m_pad = m_pad_for(M, tile_n);
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1); it splits K evenly.
-    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad != 128 &&   // no persistent m_pad 128 instance
+    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad <= 64 &&   // no persistent m_pad 96 / 128 instance
                       kbt % split_k == 0 && split_k != 3;
     int tiles = (N + tile_n - 1) / tile_n;            // the last tile may be partial
     int clusters = tiles;
@@ -516,7 +518,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     pick();
     if (tile_n == 128 && (fp > kMaxSmemPerCta || !kernel_for(tile_n, m_pad, split_k, false))) {
         // e.g. m_pad 64 with split_k 8: the 128-column mailbox does not fit, or
-        // m_pad 128 with split_k 4: no 128-column instance; use 64 columns
+        // m_pad 96 / 128 with split_k 4: no 128-column instance; use 64 columns
         tile_n = 64;
         m_pad = m_pad_of(M);
         tiles = (N + tile_n - 1) / tile_n;

@@ -458,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_reduce = bar_acc + 16u;                     // owner's mailbox barrier
     const uint32_t bar_reduce2 = bar_acc + 24u;                    // second half of the mailbox (two-phase)
     const uint32_t bar_open = bar_acc + 32u;                       // peers: the owner's ring is drained (alias)
-    // m_pad 128: one mailbox barrier per 32-column chunk (bar_reduce,
-    // bar_reduce2, bar_reduce3, bar_reduce4), so the owner reduces chunk c
-    // while the later chunks are still arriving.
+    // m_pad 96 and 128: one mailbox barrier per 32-column chunk (bar_reduce,
+    // bar_reduce2, bar_reduce3, and bar_reduce4 at m_pad 128), so the owner
+    // reduces chunk c while the later chunks are still arriving.
     const uint32_t bar_reduce3 = bar_acc + 40u;
     const uint32_t bar_reduce4 = bar_acc + 48u;
     // m_pad 64 with the mailbox in the ring, or with split_k above 2, splits
@@ -489,11 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rs) {                          // arm this rank's half: the other rank sends half a tile
             ptx::mbar_arrive_expect_tx(bar_reduce, kSlotBytes / 2);
         } else if (SPLIT_K > 1 && rank == 0) {   // arm the mailbox: every peer sends one full partial tile
-            if (M_PAD == 128) {
-                ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 4);
-                ptx::mbar_arrive_expect_tx(bar_reduce2, (SPLIT_K - 1) * kSlotBytes / 4);
-                ptx::mbar_arrive_expect_tx(bar_reduce3, (SPLIT_K - 1) * kSlotBytes / 4);
-                ptx::mbar_arrive_expect_tx(bar_reduce4, (SPLIT_K - 1) * kSlotBytes / 4);
+            if (M_PAD > 64) {              // one barrier per 32-column chunk (three or four)
+                constexpr uint32_t kChunkTx = (SPLIT_K - 1) * kTileN * 32u * 4u;
+                ptx::mbar_arrive_expect_tx(bar_reduce, kChunkTx);
+                ptx::mbar_arrive_expect_tx(bar_reduce2, kChunkTx);
+                ptx::mbar_arrive_expect_tx(bar_reduce3, kChunkTx);
+                if (M_PAD == 128)
+                    ptx::mbar_arrive_expect_tx(bar_reduce4, kChunkTx);
             } else if (kTwoPhase) {
                 ptx::mbar_arrive_expect_tx(bar_reduce, (SPLIT_K - 1) * kSlotBytes / 2);
                 ptx::mbar_arrive_expect_tx(bar_reduce2, (SPLIT_K - 1) * kSlotBytes / 2);
@@ -920,15 +922,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.timeline[4 * blockIdx.x + 3] = ptx::globaltimer();
             }
         } else {
-            // m_pad 128: two 128-column accumulators do not fit in registers, so
-            // the epilogue works in 32-column chunks.  Each chunk of the mailbox
+            // m_pad 96 and 128: two such accumulators do not fit in registers,
+            // so the epilogue works in 32-column chunks.  Each chunk of the mailbox
             // has its own barrier: a peer credits chunk c's barrier with its
             // chunk-c stores, and the owner waits for chunk c only when it
             // reduces it, while the later chunks are still arriving.  Every
             // thread makes its second (TMEM-release) arrival only after its last
             // chunk's tcgen05.wait::ld.
             constexpr int kCh = 32;
-            static_assert(M_PAD == 4 * kCh, "one mailbox barrier per 32-column chunk");
+            static_assert(M_PAD == 3 * kCh || M_PAD == 4 * kCh, "one mailbox barrier per 32-column chunk");
             const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
             int row;
             const bool valid = tmem_row_of_thread<TILE_N>(quarter, lane, row);   // row = n within the tile

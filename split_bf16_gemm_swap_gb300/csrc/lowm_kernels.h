@@ -19,5 +19,7 @@ KernelFn kernel_tile128(int m_pad, int split_k, bool persistent);
 // m_pad 128 (one-tile schedule): tile_n 64 with split_k 1, 2, 3, 4; tile_n 128
 // with split_k 1, 2, 3; nullptr otherwise.
 KernelFn kernel_mpad128(int tile_n, int split_k);
+// m_pad 96 (65 <= M <= 96), the same instances as m_pad 128.
+KernelFn kernel_mpad96(int tile_n, int split_k);
 
 }  // namespace lowm

@@ -258,14 +258,14 @@ def test_persistent_schedule_has_one_issuer(L, monkeypatch):
         assert t["mma_issuers"] == 1
 
 
-@pytest.mark.parametrize("M", [65, 96, 127, 128])
-def test_m_up_to_128_pads_to_128(L, M, monkeypatch):
-    monkeypatch.setenv("LOWM_PERSISTENT", "1")      # no persistent m_pad 128 instance: ignored
+@pytest.mark.parametrize("M,m_pad", [(65, 96), (96, 96), (97, 128), (127, 128), (128, 128)])
+def test_m_up_to_128_pads_to_96_or_128(L, M, m_pad, monkeypatch):
+    monkeypatch.setenv("LOWM_PERSISTENT", "1")      # no persistent m_pad 96 / 128 instance: ignored
     for sk in (1, 2, 3, 4):
         st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, sk)
-        assert st == lowm.LOWM_OK and t["m_pad"] == 128 and t["persistent"] == 0 and t["mma_issuers"] == 2
+        assert st == lowm.LOWM_OK and t["m_pad"] == m_pad and t["persistent"] == 0 and t["mma_issuers"] == 2
         assert t["smem_bytes"] <= 232448
-        assert t["mbox_in_ring"] == (1 if sk > 1 else 0)       # the 32-64 KiB slots share the drained ring
+        assert t["mbox_in_ring"] == (1 if sk > 1 else 0)       # the 24-64 KiB slots share the drained ring
     st, t = lowm.lowm_gemm_query_tactic(M, 64, 8192, 0)   # one tile: auto split stops where the mailbox fits
     assert st == lowm.LOWM_OK and t["split_k"] == 4
 
@@ -367,15 +367,17 @@ def test_the_header_is_c99_and_links_against_the_library(L, tmp_path):
     assert [int(x) for x in out.stdout.split()] == want
 
 
-@pytest.mark.parametrize("M", [96, 128])
-def test_m_pad_128_tactic_is_the_measured_best(L, M):
-    # GB300 sweep at N6144 K4096 with the L2 prefetch: 128-column tiles,
-    # split_k 2, the mailbox in the drained ring, 2 x 3 ring: 14.1 us, against
-    # 15.8 us for split_k 1 on 64-column tiles and 15.8-18.2 us for other rings.
+@pytest.mark.parametrize("M,kbs,stages", [(80, 4, 2), (96, 4, 2), (128, 2, 3)])
+def test_m_pad_96_and_128_tactics_are_the_measured_best(L, M, kbs, stages):
+    # GB300 sweeps at N6144 K4096: 128-column tiles, split_k 2, the mailbox in
+    # the drained ring.  m_pad 128: 2 x 3 ring, 14.1 us against 15.8 us for
+    # split_k 1 on 64-column tiles and 15.8-18.2 us for other rings.  m_pad 96:
+    # 4 x 2 ring, M96 11.84 us (12.97 us on m_pad 128), against 12.30 for 2 x
+    # 3 or 2 x 4 and 16.7 for 1 x 6.
     st, t = lowm.lowm_gemm_query_tactic(M, 6144, 4096, 0)
     assert st == lowm.LOWM_OK
     assert (t["tile_n"], t["split_k"], t["kb_per_stage"], t["stages"], t["ctas"], t["mbox_in_ring"]) == \
-        (128, 2, 2, 3, 96, 1)
+        (128, 2, kbs, stages, 96, 1)
 
 
 @pytest.mark.parametrize("K,sk", [(64 * 3, 2), (64 * 7, 3), (4096, 3), (64 * 50, 3), (64 * 9, 4)])

@@ -568,11 +568,12 @@ def test_largest_k_and_split():
     check(A, W, 8)
 
 
-# ---------------------------------------------------------------- 65 <= M <= 128 (m_pad 128, chunked epilogue)
+# ---------------------------------------------------------------- 65 <= M <= 128 (m_pad 96 / 128, chunked epilogue)
 MBIG = [
-    # M, N, K, split_k: every split with an m_pad 128 instance, ragged M and N, ring wrap-around
+    # M, N, K, split_k: every split with an m_pad 96 or 128 instance, ragged M and N, ring wrap-around
     (65, 192, 1024, 1), (80, 256, 2048, 2), (96, 640, 1024, 4), (127, 130, 512, 2), (128, 128, 4096, 1),
-    (100, 4095, 256, 1), (128, 6144, 4096, 0),
+    (100, 4095, 256, 1), (128, 6144, 4096, 0), (96, 6144, 4096, 0), (72, 2000, 1024, 3), (90, 1024, 2048, 2),
+    (97, 640, 1024, 3),
 ]
 
 
@@ -582,24 +583,26 @@ def test_m_up_to_128_random(M, N, K, split_k):
     check(A, W, split_k)
 
 
+@pytest.mark.parametrize("M", [96, 128])
 @pytest.mark.parametrize("tile,split_k", [("64", 1), ("64", 2), ("64", 4), ("128", 1), ("128", 2)])
-def test_m_up_to_128_integer_exact(tile, split_k, monkeypatch):
+def test_m_up_to_128_integer_exact(M, tile, split_k, monkeypatch):
     monkeypatch.setenv("LOWM_TILE_N", tile)
-    M, N, K = 128, 1024, 4096
+    N, K = 1024, 4096
     st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
-    assert st == lowm.LOWM_OK and t["tile_n"] == int(tile) and t["m_pad"] == 128
+    assert st == lowm.LOWM_OK and t["tile_n"] == int(tile) and t["m_pad"] == M
     A, W = inputs.make_problem(M, N, K, seed=17, kind="int")
     C = check(A, W, split_k, exact=True)
     col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
     assert np.array_equal(C, np.broadcast_to(inputs.bits(col[None, :]), C.shape))
 
 
-@pytest.mark.parametrize("tile,split_k", [("64", 1), ("64", 4), ("128", 2)])
-def test_identity_weight_m128_maps_every_row_and_column(tile, split_k, monkeypatch):
+@pytest.mark.parametrize("M", [96, 128])
+@pytest.mark.parametrize("tile,split_k", [("64", 1), ("64", 4), ("128", 2), ("128", 3)])
+def test_identity_weight_m128_maps_every_row_and_column(M, tile, split_k, monkeypatch):
     # Distinct rows of A (integers) and W = I: C[m, n] = A[m, n] exactly, which
-    # pins the m_pad 128 column chunks of the accumulators and the mailbox.
+    # pins the m_pad 96 / 128 column chunks of the accumulators and the mailbox.
     monkeypatch.setenv("LOWM_TILE_N", tile)
-    M, N, K = 128, 512, 512
+    N, K = 512, 512
     A = ((torch.arange(M * K, dtype=torch.float32).reshape(M, K) * 7) % 251 - 125).to(torch.bfloat16)
     W = torch.zeros((N, K), dtype=torch.bfloat16)
     W[torch.arange(N), torch.arange(N)] = 1.0
@@ -608,8 +611,9 @@ def test_identity_weight_m128_maps_every_row_and_column(tile, split_k, monkeypat
     assert np.array_equal(F, A.to(torch.float64).numpy()[:, :N])
 
 
-def test_m128_twenty_launches_are_bitwise_identical():
-    M, N, K, split_k = 128, 6144, 4096, 2
+@pytest.mark.parametrize("M", [96, 128])
+def test_m128_twenty_launches_are_bitwise_identical(M):
+    N, K, split_k = 6144, 4096, 2
     A, W = inputs.make_problem(M, N, K, seed=33)
     Ad, Wd = A.to(DEV), W.to(DEV)
     outs = torch.empty((20, M, N), dtype=torch.bfloat16, device=DEV)
