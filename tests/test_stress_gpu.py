@@ -186,3 +186,33 @@ def test_stress_with_the_w_promise(M, N, K, split_k):
         outs, probes = stressed(Ad, Wd, M, N, K, split_k, stall_ns, flags=flags)
         assert bool((outs.view(torch.int16) == ref.view(torch.int16)[None]).all())
         check_probes(probes)
+
+
+SOAK_CONFIGS = [  # M, N, K, split_k, flags
+    (4, 6144, 4096, 2, 1), (4, 6144, 4096, 2, 0), (64, 6144, 4096, 2, 1), (96, 6144, 4096, 2, 1),
+    (128, 6144, 4096, 2, 1), (4, 2304, 12288, 4, 1), (16, 6144, 32768, 4, 1), (64, 6144, 4096, 3, 0),
+    (4, 49152, 4096, 2, 1), (32, 4096, 4096, 0, 1)]
+
+
+@pytest.mark.parametrize("M,N,K,split_k,flags", SOAK_CONFIGS)
+def test_soak(M, N, K, split_k, flags):
+    # The extended soak: LOWM_SOAK_ROUNDS rounds (unset: skipped) of the four
+    # stall patterns (warps 4 and 5, the second issuer, or all three; 5 or
+    # 50 us) with the TMEM hog, 20 launches each, integer inputs against the
+    # closed form.  80 rounds are 6,400 launches per configuration.
+    import os
+    rounds = int(os.environ.get("LOWM_SOAK_ROUNDS", "0"))
+    if rounds <= 0:
+        pytest.skip("set LOWM_SOAK_ROUNDS to run the extended soak")
+    A, W = inputs.make_problem(M, N, K, seed=4242, kind="int")
+    Ad, Wd = A.to(DEV), W.to(DEV)
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    want = np.broadcast_to(inputs.bits(col[None, :]), (M, N))
+    stalls = [(STALL_WARPS, 5_000), (STALL_WARPS, 50_000), (1 << 6, 5_000), (STALL_WARPS | (1 << 6), 50_000)]
+    differing = 0
+    for _ in range(rounds):
+        for warp_mask, stall_ns in stalls:
+            outs, probes = stressed(Ad, Wd, M, N, K, split_k, stall_ns, warp_mask=warp_mask, flags=flags)
+            differing += int((inputs.bits(outs.cpu()) != want[None]).any(axis=(1, 2)).sum())
+            check_probes(probes)
+    assert differing == 0, "%d of %d launches differ from the closed form" % (differing, rounds * len(stalls) * LAUNCHES)
