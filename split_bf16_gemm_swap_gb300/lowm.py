@@ -179,8 +179,12 @@ def lowm_tmem_hog_launch(stream=None, ctas: int = 1024, ncols: int = 256, iters:
     return lib().lowm_tmem_hog_launch(_stream(stream), int(ctas), int(ncols), int(iters))
 
 
-def gemm(A, W, C=None, split_k: int = 0, stream=None):
-    """C = A . W^T for CUDA bf16 tensors A [M,K], W [N,K]; allocates C if not given."""
+def gemm(A, W, C=None, split_k: int = 0, stream=None, flags: int = 0):
+    """C = A . W^T for CUDA bf16 tensors A [M,K], W [N,K]; allocates C if not given.
+
+    flags: LOWM_FLAG_* for lowm_gemm_bf16_ex (LOWM_FLAG_W_BEFORE_PDL_WAIT when
+    the kernel that precedes this launch on the stream does not write W).
+    """
     import torch
     if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise TypeError("A and W must be bfloat16")
@@ -192,7 +196,7 @@ def gemm(A, W, C=None, split_k: int = 0, stream=None):
     N = W.shape[0]
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    s = lowm_gemm_bf16(A, W, C, M, N, K, split_k, stream)
+    s = lowm_gemm_bf16_ex(A, W, C, M, N, K, split_k, flags, stream)
     if s != LOWM_OK:
-        raise LowmError(s, "lowm_gemm_bf16")
+        raise LowmError(s, "lowm_gemm_bf16_ex")
     return C

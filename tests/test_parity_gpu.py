@@ -652,6 +652,12 @@ def test_python_gemm_wrapper_allocates_and_raises():
     assert lowm.gemm(A.to(DEV), W.to(DEV), C2, split_k=2) is C2
     sync_ok()
     assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    C3 = lowm.gemm(A.to(DEV), W.to(DEV), split_k=2, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)   # the W promise
+    sync_ok()
+    assert torch.equal(C.view(torch.int16), C3.view(torch.int16))
+    with pytest.raises(lowm.LowmError) as e:
+        lowm.gemm(A.to(DEV), W.to(DEV), split_k=2, flags=2)                 # unknown flag bit
+    assert e.value.status == lowm.LOWM_ERR_INVALID_ARGUMENT
     with pytest.raises(lowm.LowmError) as e:
         lowm.gemm(A.to(DEV)[:, :96].contiguous(), W.to(DEV)[:, :96].contiguous(), split_k=1)   # K = 96: not a multiple of 64
     assert e.value.status == lowm.LOWM_ERR_UNSUPPORTED_SHAPE
