@@ -52,6 +52,7 @@ OTHER_CONFIGS = [
     ("M16 N6144 K4096 auto", (16, 6144, 4096, 0)),
     ("M32 N6144 K4096 auto", (32, 6144, 4096, 0)),
     ("M64 N6144 K4096 auto", (64, 6144, 4096, 0)),
+    ("M96 N6144 K4096 auto", (96, 6144, 4096, 0)),
     ("M128 N6144 K4096 auto", (128, 6144, 4096, 0)),
 ]
 FALLBACK_HBM_GBS = 6800.0
