@@ -387,6 +387,15 @@ def run_ours(args):
         "us_per_gemm": vsecs / vsteps * 1e6, "gbs": bytes_per * vsteps / vsecs / 1e9,
         "frac": bytes_per * vsteps / vsecs / 1e9 / peak, "steps": vsteps,
         "entry_point": "lowm_gemm_bf16_ex(flags=%d)" % vw["flags"]}
+    # GEMMs that share their input (A is not written by the preceding kernel
+    # either, as for projections of the same activations): both promises.
+    both = lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT | lowm.LOWM_FLAG_A_BEFORE_PDL_WAIT
+    aw = dict(w, flags=both)
+    asecs, _, _ = time_device(lowm, aw, vsteps, max(args.warmup, 3), device)
+    variants["w_and_a_before_pdl_wait"] = {
+        "us_per_gemm": asecs / vsteps * 1e6, "gbs": bytes_per * vsteps / asecs / 1e9,
+        "frac": bytes_per * vsteps / asecs / 1e9 / peak, "steps": vsteps,
+        "entry_point": "lowm_gemm_bf16_ex(flags=%d)" % both}
 
     # The other configurations of the method's workloads (split-K reduction
     # width, long K, the M sweep, M above 64), same protocol and launch flags,

@@ -176,6 +176,17 @@ lowm_status_t lowm_gemm_bf16(const void *A, const void *W, void *C,
 #define LOWM_FLAG_W_BEFORE_PDL_WAIT 1u
 
 /*
+ * LOWM_FLAG_A_BEFORE_PDL_WAIT: the caller promises that A is not written by
+ * the kernel that precedes this launch in the stream either (GEMMs that share
+ * one input, such as projections of the same activations).  The kernel then
+ * loads A without waiting for the preceding kernel; only its stores of C wait
+ * for it.  It takes effect together with LOWM_FLAG_W_BEFORE_PDL_WAIT (alone,
+ * W is still read after the wait, and so is A).  Breaking the promise gives
+ * undefined results.
+ */
+#define LOWM_FLAG_A_BEFORE_PDL_WAIT 2u
+
+/*
  * lowm_gemm_bf16 with launch flags (a bitwise OR of LOWM_FLAG_*; unknown bits
  * are rejected with LOWM_ERR_INVALID_ARGUMENT).  flags == 0 is lowm_gemm_bf16.
  */

@@ -7,7 +7,7 @@ does not load the library; the first call does, and fails loudly if it is
 missing.
 """
 from .lowm import (  # noqa: F401
-    ABI_FUNCTIONS, LOWM_FLAG_W_BEFORE_PDL_WAIT, LOWM_OK, LowmError, gemm, lowm_gemm_bf16, lowm_gemm_bf16_debug,
-    lowm_gemm_bf16_ex, lowm_gemm_bf16_host,
+    ABI_FUNCTIONS, LOWM_FLAG_A_BEFORE_PDL_WAIT, LOWM_FLAG_W_BEFORE_PDL_WAIT, LOWM_OK, LowmError, gemm,
+    lowm_gemm_bf16, lowm_gemm_bf16_debug, lowm_gemm_bf16_ex, lowm_gemm_bf16_host,
     lowm_gemm_query_tactic, lowm_gemm_query_tactic_ex, lowm_gemm_sync_status, lowm_status_string, lowm_tmem_hog_launch,
 )

@@ -683,7 +683,7 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K, int split_k, void *stream,
                      const lowm_debug_opts_t *dbg, unsigned int flags = 0)
 {
-    if (flags & ~LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    if (flags & ~(LOWM_FLAG_W_BEFORE_PDL_WAIT | LOWM_FLAG_A_BEFORE_PDL_WAIT))
         return LOWM_ERR_INVALID_ARGUMENT;
     if (!A || !W || !C)
         return LOWM_ERR_INVALID_ARGUMENT;
@@ -735,6 +735,10 @@ lowm_status_t launch(const void *A, const void *W, void *C, int M, int N, int K,
     p.w_prefetch_stages = (uint32_t)t.w_prefetch_stages;   // 0 unless the flag is set
     p.l2_prefetch_stages = (uint32_t)t.l2_prefetch_stages;
     p.l2_before_wait_stages = (uint32_t)t.l2_before_wait_stages;
+    // Loads skip the dependency wait only when neither operand is written by
+    // the preceding kernel (both promises); C still waits in the epilogue.
+    constexpr unsigned kBoth = LOWM_FLAG_W_BEFORE_PDL_WAIT | LOWM_FLAG_A_BEFORE_PDL_WAIT;
+    p.a_before_wait = (flags & kBoth) == kBoth ? 1u : 0u;
     if (dbg) {
         p.stall_warp_mask = dbg->stall_warp_mask;
         p.stall_rank_mask = dbg->stall_rank_mask;
@@ -816,7 +820,7 @@ lowm_status_t lowm_gemm_query_tactic_ex(int M, int N, int K, int split_k, unsign
 {
     if (!out)
         return LOWM_ERR_INVALID_ARGUMENT;
-    if (flags & ~LOWM_FLAG_W_BEFORE_PDL_WAIT)
+    if (flags & ~(LOWM_FLAG_W_BEFORE_PDL_WAIT | LOWM_FLAG_A_BEFORE_PDL_WAIT))
         return LOWM_ERR_INVALID_ARGUMENT;
     // Host-only query: with a usable sm_103 device current, the same numbers the
     // launch uses; otherwise the per-SM arithmetic for a 152-SM GB300.

@@ -110,6 +110,7 @@ struct KernelParams {
     uint32_t l2_prefetch_stages;  // W stages requested into L2 ahead of the newest ring load (0: none)
     uint32_t l2_before_wait_stages;   // W stages requested into L2 before the programmatic-dependency
                                       // wait (0 when the W promise requests the ring itself early)
+    uint32_t a_before_wait;       // 1: the caller promised the preceding kernel does not write A either
     unsigned long long *probes;     // [kProbeWords * ctas], see lowm_debug_opts_t
     float *c_f32;
     unsigned long long *timeline;   // [4 * ctas]: prologue end, first / last full stage, epilogue end
@@ -564,7 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int l2w = pre > 0 ? 0 : (n_stages < (int)p.l2_before_wait_stages ? n_stages : (int)p.l2_before_wait_stages);
             for (int i = 0; i < l2w; ++i)
                 ptx::tma_prefetch_3d(&tmap_w, 0, n0, kb0 + i * kbs);
-            ptx::griddep_wait();          // A (and C) may belong to the previous kernel in the stream
+            // A may belong to the previous kernel in the stream, unless the
+            // caller promised otherwise (then only C waits, in the epilogue).
+            if (!p.a_before_wait)
+                ptx::griddep_wait();
             for (int i = 0; i < pre; ++i)
                 ptx::tma_load_3d(sbase + L.a + (uint32_t)i * a_stage_bytes, &tmap_a, 0, 0, kb0 + i * kbs,
                                  bar_full + 8u * i, pol_a);

@@ -24,6 +24,7 @@ LOWM_ERR_CUDA = 5
 LOWM_ERR_TIMEOUT = 6
 
 LOWM_FLAG_W_BEFORE_PDL_WAIT = 1
+LOWM_FLAG_A_BEFORE_PDL_WAIT = 2
 
 # Exported C functions, in header order.
 ABI_FUNCTIONS = (

@@ -154,7 +154,7 @@ def test_ring_without_the_w_promise(L, M, N, K, sk, tile, kbs, stages, alias):
 
 
 def test_query_with_unknown_flags_is_rejected(L):
-    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, 2)
+    st, t = lowm.lowm_gemm_query_tactic_ex(4, 6144, 4096, 2, 4)
     assert st == lowm.LOWM_ERR_INVALID_ARGUMENT and t is None
 
 
@@ -312,7 +312,7 @@ def test_gemm_rejects_null_and_misaligned_pointers_before_touching_a_device(L):
         == lowm.LOWM_ERR_INVALID_ARGUMENT
     assert lowm.lowm_gemm_bf16_host(0, 1, 1, 1, 1, 1, 4, 64, 64, 0, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
     assert lowm.lowm_tmem_hog_launch(0, 1, 48, 1) == lowm.LOWM_ERR_INVALID_ARGUMENT
-    assert lowm.lowm_gemm_bf16_ex(0x1000, 0x100000, 0x200000, 4, 64, 64, 1, 2, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
+    assert lowm.lowm_gemm_bf16_ex(0x1000, 0x100000, 0x200000, 4, 64, 64, 1, 4, 0) == lowm.LOWM_ERR_INVALID_ARGUMENT
 
 
 def test_library_does_not_reference_the_oracle():
@@ -337,7 +337,7 @@ int main(void)
            t.mma_issuers, t.w_prefetch_stages);
     if (lowm_gemm_query_tactic(129, 64, 64, 1, &t) != LOWM_ERR_UNSUPPORTED_SHAPE) return 2;
     if (lowm_gemm_bf16(0, 0, 0, 4, 64, 64, 1, 0) != LOWM_ERR_INVALID_ARGUMENT) return 3;
-    if (lowm_gemm_bf16_ex((void *)0x1000, (void *)0x2000, (void *)0x3000, 4, 64, 64, 1, 2u, 0)
+    if (lowm_gemm_bf16_ex((void *)0x1000, (void *)0x2000, (void *)0x3000, 4, 64, 64, 1, 4u, 0)
         != LOWM_ERR_INVALID_ARGUMENT) return 4;      /* unknown flag bit */
     return 0;
 }

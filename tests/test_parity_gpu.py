@@ -656,7 +656,7 @@ def test_python_gemm_wrapper_allocates_and_raises():
     sync_ok()
     assert torch.equal(C.view(torch.int16), C3.view(torch.int16))
     with pytest.raises(lowm.LowmError) as e:
-        lowm.gemm(A.to(DEV), W.to(DEV), split_k=2, flags=2)                 # unknown flag bit
+        lowm.gemm(A.to(DEV), W.to(DEV), split_k=2, flags=4)                 # unknown flag bit
     assert e.value.status == lowm.LOWM_ERR_INVALID_ARGUMENT
     with pytest.raises(lowm.LowmError) as e:
         lowm.gemm(A.to(DEV)[:, :96].contiguous(), W.to(DEV)[:, :96].contiguous(), split_k=1)   # K = 96: not a multiple of 64
@@ -865,6 +865,32 @@ def test_auto_tactics_of_the_tile_sweep(M, N, K, tile, split_k):
     C1 = check(A, W, 0, flags=lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT)
     C0, _ = run_gpu(A, W, 0, want_f32=False)
     assert np.array_equal(C0, C1)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(4, 6144, 4096, 2), (64, 6144, 4096, 0), (4, 2304, 12288, 4),
+                                           (96, 1024, 2048, 2), (3, 200, 640, 3)])
+def test_gemms_sharing_a_with_both_promises(M, N, K, split_k):
+    # Projections of one input: A is shared and never written, each GEMM has
+    # its own W, launched back to back with both promises (A and W loaded
+    # without waiting for the preceding GEMM; only C waits).  Each output
+    # equals a launch without flags on the same operands, and the first one
+    # meets the parity bar.
+    both = lowm.LOWM_FLAG_W_BEFORE_PDL_WAIT | lowm.LOWM_FLAG_A_BEFORE_PDL_WAIT
+    A, _ = inputs.make_problem(M, N, K, seed=91)
+    Ws = [inputs.make_problem(M, N, K, seed=92 + i)[1] for i in range(4)]
+    Ad = A.to(DEV)
+    Wd = [w.to(DEV) for w in Ws]
+    Cs = [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV) for _ in Ws]
+    for w, c in zip(Wd, Cs):
+        assert lowm.lowm_gemm_bf16_ex(Ad, w, c, M, N, K, split_k, both, None) == lowm.LOWM_OK
+    sync_ok()
+    for w, c in zip(Wd, Cs):
+        ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+        assert lowm.lowm_gemm_bf16(Ad, w, ref, M, N, K, split_k, None) == lowm.LOWM_OK
+        sync_ok()
+        assert torch.equal(ref.view(torch.int16), c.view(torch.int16))
+    C = check(A, Ws[0], split_k, flags=both)
+    assert np.array_equal(C, inputs.bits(Cs[0].cpu()))
 
 
 def test_pdl_chain_with_the_deep_ring_and_w_promise():
