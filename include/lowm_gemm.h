@@ -61,10 +61,10 @@ typedef enum {
  *                mapped onto the tensor core's M, the tiny M onto its N): 128
  *                when N % 128 == 0, split_k <= 4 and the 128-column grid has
  *                64 CTAs to two per SM, each streaming at most 768 KiB of W
- *                unless every SM gets one (at m_pad >= 64 also: the
+ *                unless every SM gets one (at m_pad >= 48 also: the
  *                64-column grid would not fit one CTA per SM, and split_k 2
  *                or one CTA per SM); else 64
- *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 64, 96 or 128;
+ *   m_pad        M rounded up to the MMA's N granularity (8, 16, 32, 48, 64, 96 or 128;
  *                at least 16 for 128-column tiles); rows M..m_pad-1 are
  *                zero-filled by the TMA unit and never stored
  *   split_k      CTAs per cluster along K (1, 2, 3, 4 or 8).  K is cut into

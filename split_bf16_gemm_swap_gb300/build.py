@@ -1,11 +1,11 @@
 """Compile the CUDA library ``liblowm_gemm.so`` in-tree for sm_103a.
 
-Five translation units compiled in parallel with nvcc (one ``-gencode``,
+Six translation units compiled in parallel with nvcc (one ``-gencode``,
 no CMake): the host launcher and C ABI (``csrc/lowm_gemm.cu``) and the kernel
 instances for 64- and 128-column tiles (``csrc/kernels_tile64.cu``,
-``csrc/kernels_tile128.cu``) and for m_pad 128 and 96
-(``csrc/kernels_mpad128.cu``, ``csrc/kernels_mpad96.cu``), then linked into
-one shared library.
+``csrc/kernels_tile128.cu``) and for m_pad 128, 96 and 48
+(``csrc/kernels_mpad128.cu``, ``csrc/kernels_mpad96.cu``,
+``csrc/kernels_mpad48.cu``), then linked into one shared library.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "liblowm_gemm.so")
 CSRC = os.path.join(HERE, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in ("lowm_gemm.cu", "kernels_tile64.cu", "kernels_tile128.cu",
-                                           "kernels_mpad128.cu", "kernels_mpad96.cu")]
+                                           "kernels_mpad128.cu", "kernels_mpad96.cu", "kernels_mpad48.cu")]
 DEPS = SOURCES + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [
     os.path.join(ROOT, "include", "lowm_gemm.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

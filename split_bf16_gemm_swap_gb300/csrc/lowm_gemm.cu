@@ -126,7 +126,7 @@ int env_int(const char *name, int dflt)
 
 int m_pad_of(int M)
 {
-    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 96 ? 96 : 128;
+    return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : M <= 64 ? 64 : M <= 96 ? 96 : 128;
 }
 
 int footprint(int tile_n, int m_pad, int split_k, int stages, int kbs, int bufs, bool alias = false)
@@ -226,7 +226,7 @@ bool shape_ok(int M, int N, int K, int split_k)
 //   - has at least 64 CTAs (enough concurrent streams to fill HBM) and at
 //     most two per SM,
 //   - streams at most 768 KiB of W per CTA or has a CTA on every SM,
-//   - and, at m_pad 64 and above, replaces a 64-column grid that would not
+//   - and, at m_pad 48 and above, replaces a 64-column grid that would not
 //     fit one CTA per SM, with split_k 2 or one CTA per SM (the m_pad 64
 //     mailbox of three 128-column partials leaves too small a ring);
 // 64 columns otherwise.  Measured on GB300 with the W promise, 64 -> 128
@@ -260,7 +260,7 @@ int choose_tile_n(int M, int N, int K, int split_k, int sms)
         return 64;
     const long long c64 = (long long)((N + 63) / 64) * split_k, c128 = (long long)(N / 128) * split_k;
     const double per_cta = 2.0 * N * (double)K / (double)c128;
-    const bool wide_pad = m_pad_of(M) >= 64;
+    const bool wide_pad = m_pad_of(M) >= 48;
     const bool ok = c128 >= kMinStreams && c128 <= 2LL * sms && (per_cta <= kLongStreamBytes || c128 >= sms) &&
                     (!wide_pad || (c64 > sms && (split_k <= 2 || c128 <= sms)));
     return ok ? 128 : 64;
@@ -361,6 +361,8 @@ KernelFn kernel_for(int tile_n, int m_pad, int sk, bool persistent)
         return persistent ? nullptr : lowm::kernel_mpad128(tile_n, sk);
     if (m_pad == 96)
         return persistent ? nullptr : lowm::kernel_mpad96(tile_n, sk);
+    if (m_pad == 48)
+        return persistent ? nullptr : lowm::kernel_mpad48(tile_n, sk);
     if (tile_n == 64)
         return lowm::kernel_tile64(m_pad, sk, persistent);
     if (tile_n == 128)
@@ -470,7 +472,7 @@ lowm_status_t make_tactic(int M, int N, int K, int split_k, int sms, bool have_d
     int tile_n = choose_tile_n(M, N, K, split_k, nsm);
     int m_pad = m_pad_for(M, tile_n);
     // The persistent schedule is opt-in (LOWM_PERSISTENT=1); it splits K evenly.
-    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad <= 64 &&   // no persistent m_pad 96 / 128 instance
+    bool persistent = env_int("LOWM_PERSISTENT", 0) == 1 && m_pad <= 64 && m_pad != 48 &&   // no persistent m_pad 48 / 96 / 128 instance
                       kbt % split_k == 0 && split_k != 3;
     int tiles = (N + tile_n - 1) / tile_n;            // the last tile may be partial
     int clusters = tiles;

@@ -130,8 +130,8 @@ struct SmemLayout {
 // writes the owner's mailbox only after the owner has said so; see
 // lowm_splitk_kernel), so a split-K CTA needs max(ring, mailbox + staging)
 // bytes rather than their sum.
-// Split-K 2 at m_pad 64 with the mailbox next to the ring reduces and
-// scatters: rank q keeps rows [32 q, 32 q + 32) of the tile, sends the other
+// Split-K 2 at m_pad 48 and 64 with the mailbox next to the ring reduces and
+// scatters: rank q keeps rows [q m_pad / 2, (q + 1) m_pad / 2) of the tile, sends the other
 // half of its partial to the other rank, sums its own half in rank order and
 // stores it.  Both directions of the cluster link carry 16 KiB (128-column
 // tiles) at once instead of one carrying 32 KiB, neither rank waits for the
@@ -142,7 +142,7 @@ struct SmemLayout {
 // not used.
 __host__ __device__ constexpr bool reduce_scatter_of(int m_pad, int split_k, int bufs, bool mbox_in_ring)
 {
-    return split_k == 2 && bufs == 1 && !mbox_in_ring && m_pad == 64;
+    return split_k == 2 && bufs == 1 && !mbox_in_ring && (m_pad == 48 || m_pad == 64);
 }
 
 __host__ __device__ inline uint32_t ring_bytes_of(int tile_n, int m_pad, int stages, int kb_per_stage)

@@ -21,5 +21,8 @@ KernelFn kernel_tile128(int m_pad, int split_k, bool persistent);
 KernelFn kernel_mpad128(int tile_n, int split_k);
 // m_pad 96 (65 <= M <= 96), the same instances as m_pad 128.
 KernelFn kernel_mpad96(int tile_n, int split_k);
+// m_pad 48 (33 <= M <= 48), one-tile schedule, split_k 1, 2, 3, 4, 8 at both
+// tile widths.
+KernelFn kernel_mpad48(int tile_n, int split_k);
 
 }  // namespace lowm

@@ -250,12 +250,12 @@ def test_a_dropped_two_phase_mailbox_times_out(M, split_k):
 @pytest.mark.parametrize("M,N,flags", [(33, 6144, 1), (40, 6144, 0), (47, 256, 0), (48, 6144, 1), (63, 200, 0),
                                        (64, 6144, 0), (64, 6144, 1), (64, 6150, 1), (64, 70, 0), (64, 1, 0)])
 def test_reduce_scatter_rows(M, N, flags):
-    # Each rank keeps half of the 64 padded rows: rank 1's half holds 1..32
-    # real rows, and 64- and 128-column tiles, N tails and both launch flags
-    # take the same exchange.
+    # Each rank keeps half of the 48 or 64 padded rows: rank 1's half holds
+    # 1..24 or 1..32 real rows, and 64- and 128-column tiles, N tails and both
+    # launch flags take the same exchange.
     K = 4096
     st, t = lowm.lowm_gemm_query_tactic_ex(M, N, K, 2, flags)
-    assert st == lowm.LOWM_OK and (t["m_pad"], t["split_k"], t["mbox_in_ring"]) == (64, 2, 0)
+    assert st == lowm.LOWM_OK and (t["m_pad"], t["split_k"], t["mbox_in_ring"]) == (48 if M <= 48 else 64, 2, 0)
     A, W = inputs.make_problem(M, N, K, seed=1400 + M + N)
     check(A, W, 2, flags=flags)
 
@@ -575,6 +575,29 @@ MBIG = [
     (100, 4095, 256, 1), (128, 6144, 4096, 0), (96, 6144, 4096, 0), (72, 2000, 1024, 3), (90, 1024, 2048, 2),
     (97, 640, 1024, 3),
 ]
+
+
+# ---------------------------------------------------------------- 33 <= M <= 48 (m_pad 48)
+@pytest.mark.parametrize("M,N,K,split_k", [(33, 192, 1024, 1), (40, 640, 2048, 2), (48, 6144, 4096, 0),
+                                           (41, 2000, 1024, 3), (48, 256, 2048, 4), (36, 192, 1024, 8),
+                                           (44, 70, 512, 2)])
+def test_m_pad_48_random(M, N, K, split_k):
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK and t["m_pad"] == 48
+    A, W = inputs.make_problem(M, N, K, seed=760 + M + N)
+    check(A, W, split_k)
+
+
+@pytest.mark.parametrize("tile,split_k", [("64", 1), ("64", 2), ("64", 8), ("128", 2), ("128", 4)])
+def test_m_pad_48_integer_exact(tile, split_k, monkeypatch):
+    monkeypatch.setenv("LOWM_TILE_N", tile)
+    M, N, K = 48, 1024, 4096
+    st, t = lowm.lowm_gemm_query_tactic(M, N, K, split_k)
+    assert st == lowm.LOWM_OK and t["tile_n"] == int(tile) and t["m_pad"] == 48
+    A, W = inputs.make_problem(M, N, K, seed=18, kind="int")
+    C = check(A, W, split_k, exact=True)
+    col = W.to(torch.int64).sum(dim=1).to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(C, np.broadcast_to(inputs.bits(col[None, :]), C.shape))
 
 
 @pytest.mark.parametrize("M,N,K,split_k", MBIG)
